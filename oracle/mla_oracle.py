@@ -350,8 +350,10 @@ def index_convert(req_id, block_table, token_indices, block_size, cu_seqlens=Non
 
     ``out[t, i] = block_table[req_id[t], idx // BS] * BS + idx % BS`` with
     ``idx = token_indices[t, i]``; ``-1`` when ``idx`` is negative or when the
-    block column ``idx // BS`` is not below the table's width. Block-table
-    values themselves are not range-checked.
+    block column ``idx // BS`` is not below the table's width. The page's
+    out-of-bounds safety rule is read as covering the row index too: a
+    request id outside the table also gives ``-1``. Block-table values
+    themselves are not range-checked.
 
     Without ``cu_seqlens`` the result is ``[T, topk]``. With ``cu_seqlens
     [T + 1]`` the first ``cu[t + 1] - cu[t]`` converted entries of row ``t``
@@ -364,8 +366,9 @@ def index_convert(req_id, block_table, token_indices, block_size, cu_seqlens=Non
     T, K = ti.shape
     cols = bt.shape[1]
     blk = np.where(ti >= 0, ti // block_size, 0)
-    ok = (ti >= 0) & (blk < cols)
-    rows = np.broadcast_to(req[:, None], ti.shape)
+    req_ok = (req >= 0) & (req < bt.shape[0])
+    ok = (ti >= 0) & (blk < cols) & req_ok[:, None]
+    rows = np.broadcast_to(np.where(req_ok, req, 0)[:, None], ti.shape)
     base = bt[rows, np.where(ok, blk, 0)]
     conv = np.where(ok, base * block_size + np.where(ti >= 0, ti % block_size, 0), -1)
     conv = conv.astype(np.int64)

@@ -353,7 +353,7 @@ def _brute_convert(req, bt, ti, bs):
     for t in range(T):
         for i in range(K):
             idx = int(ti[t, i])
-            if idx < 0 or idx // bs >= bt.shape[1]:
+            if idx < 0 or idx // bs >= bt.shape[1] or not 0 <= int(req[t]) < bt.shape[0]:
                 out[t][i] = -1
             else:
                 out[t][i] = int(bt[int(req[t]), idx // bs]) * bs + idx % bs
@@ -374,6 +374,15 @@ def test_index_convert_brute_force_and_edges():
     assert np.array_equal(got, want)
     assert got[0, 0] == -1 and got[0, 2] == -1 and got[1, 3] == -1
     assert got[0, 1] == int(bt[0, 4]) * 16 + 15
+
+
+def test_index_convert_request_outside_table():
+    bt = np.arange(8, dtype=np.int32).reshape(2, 4)
+    ti = np.array([[0, 17, -1, 63], [5, 6, 7, 8]], dtype=np.int32)
+    got = O.index_convert(np.array([2, -1], dtype=np.int32), bt, ti, 16)
+    assert np.all(got == -1)
+    got = O.index_convert(np.array([1, 0], dtype=np.int32), bt, ti, 16)
+    assert got.tolist() == [[4 * 16, 5 * 16 + 1, -1, 7 * 16 + 15], [5, 6, 7, 8]]
 
 
 def test_index_convert_ragged_output():
