@@ -1,0 +1,252 @@
+/*
+ * mla_decode.h -- C ABI of the paged MLA decode library for GB300 (sm_103a).
+ *
+ * Multi-head latent attention decode over a paged latent KV cache. Every
+ * cache slot holds one 576-wide row: c_kv (kv_lora_rank = 512 columns)
+ * followed by k_pe (64 rope columns). Scores use all 576 columns; the values
+ * are the first 512 columns of the same row. The KV sequence of every row is
+ * split into segments (split-K); each segment produces base-2 partials
+ * (max, expsum, normalised partial output) and a merge produces the output
+ * plus a natural-log LSE. Optional per-head fp32 sink logits, e4m3 fp8 q/KV
+ * with per-tensor scales, multi-token causal rows and a sparse top-k variant
+ * whose per-request positions are mapped through the block table.
+ *
+ * Sources (vLLM pages on the ROCm AITER MLA backend):
+ *   [merge]  "vllm.v1.attention.ops.rocm_aiter_mla_merge", module docstring
+ *            and merge_mla_segments_triton (partition, base-2 partials,
+ *            natural-log LSE, shapes).
+ *   [sparse] "vllm.v1.attention.backends.mla.rocm_aiter_mla_sparse":
+ *            ROCMAiterMLASparseImpl.__init__ (sinks must be fp32 [H]),
+ *            _forward_mla (sink fold, empty rows), forward_mqa (q layout,
+ *            fp8 per-tensor scales), triton_convert_req_index_to_global_index
+ *            (index formula, -1 rules, topk % 128 == 0).
+ *   [dense]  "vllm/v1/attention/backends/mla/rocm_aiter_mla.py" (source
+ *            listing): forward_mqa (q [T, H, 576], cache view), the
+ *            segmented call in _forward_segmented_dcp_verify,
+ *            _segmented_mla_page_size (tile rule) and
+ *            dcp_local_verify_row_lens (causal bound of multi-token rows).
+ *
+ * Conventions shared by every entry point:
+ *   - The caller owns all memory. Every pointer argument except the plan and
+ *     problem structs is a DEVICE pointer. The library allocates nothing and
+ *     never synchronises the stream; all work is enqueued on `stream`.
+ *   - Arguments are checked on the host before anything is launched; a bad
+ *     argument returns an error status and launches nothing. Nothing is
+ *     thrown across the ABI.
+ *   - MLA_ERR_CUDA means a launch failed (cudaGetLastError after the launch);
+ *     mla_last_cuda_error() gives the CUDA error string of the calling thread.
+ *   - Contiguous layouts unless a stride is given. Rows of q and of the cache
+ *     are 576 elements; q, kv_cache and out must be 16-byte aligned,
+ *     workspace 256-byte aligned, lse and the float/int arrays 4-byte aligned.
+ *   - Values the host cannot see (block-table entries, seq_lens, slots) are
+ *     trusted to be in range: block_table entries in [0, num_blocks),
+ *     0 <= seq_lens[r] <= max_blocks_per_req * block_size, seq_lens[r] >=
+ *     qlen_r, slots in [-1, num_blocks * block_size).
+ */
+#ifndef MLA_DECODE_H_
+#define MLA_DECODE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* a shape, pointer, alignment or enum is invalid */
+  MLA_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. head_dim != 576) */
+  MLA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the plan needs */
+  MLA_ERR_CUDA = 4           /* a CUDA launch failed; see mla_last_cuda_error() */
+} mla_status_t;
+
+typedef enum {
+  MLA_DTYPE_BF16 = 0,        /* bfloat16 */
+  MLA_DTYPE_FP8_E4M3 = 1     /* OCP e4m3fn, value = code * per-tensor scale */
+} mla_dtype_t;
+
+/* Host-side description of one decode call ([dense] forward_mqa, [sparse]
+ * forward_mqa). */
+typedef struct {
+  int32_t num_tokens;          /* T: rows of q, out and lse */
+  int32_t num_reqs;            /* R: dense requests (rows of block_table, seq_lens);
+                                  ignored by the sparse variant */
+  int32_t num_heads;           /* H, 1..128 */
+  int32_t head_dim;            /* 576 (512 + 64); other values are unsupported */
+  int32_t kv_lora_rank;        /* 512 */
+  int32_t block_size;          /* tokens per physical cache block (> 0) */
+  int32_t max_blocks_per_req;  /* columns of block_table that may be read */
+  int32_t num_blocks;          /* physical blocks in the cache */
+  int32_t max_seq_len;         /* host upper bound of seq_lens (dense) */
+  int32_t max_qlen;            /* max tokens per request; 1 when qo_indptr is NULL */
+  int32_t topk;                /* 0 = dense; > 0 = sparse, longest slot list per token */
+  int32_t q_dtype;             /* mla_dtype_t */
+  int32_t kv_dtype;            /* mla_dtype_t; must equal q_dtype */
+  int32_t has_sinks;           /* 1 when a sinks array will be passed */
+  int32_t num_segments;        /* split-K segments per row; 0 lets the planner choose */
+  int32_t num_sms;             /* SMs to plan for; 0 queries the current device */
+} mla_problem_t;
+
+/* Filled by mla_decode_plan; pass it unchanged to mla_decode_fwd or
+ * mla_decode_segments. */
+typedef struct {
+  mla_problem_t prob;
+  int32_t num_segments;        /* NS actually used (>= 1) */
+  int32_t tile_size;           /* partition unit: tiles_per_segment =
+                                  cdiv(len, NS * tile_size) ([merge] docstring) */
+  int32_t kernel;              /* decode kernel variant (internal id) */
+  int32_t rows_per_cta;        /* query rows (token x head) one CTA owns */
+  int32_t row_tiles;           /* row tiles per request (dense) or token (sparse) */
+  int32_t grid_x, grid_y, grid_z;
+  int32_t num_sms;
+  int32_t reserved[4];
+  size_t workspace_bytes;      /* bytes mla_decode_fwd needs; 0 when NS == 1 */
+  size_t segm_max_offset;      /* workspace layout: segm_output at offset 0, */
+  size_t segm_expsum_offset;   /* then segm_max, then segm_expsum (256-B aligned) */
+} mla_plan_t;
+
+/*
+ * mla_decode_plan -- choose segments, tile and launch shape for a problem.
+ * Host only: no device call other than (when prob->num_sms == 0) a query of
+ * the current device's SM count, no synchronisation.
+ * tile_size = min(128, largest power of two dividing block_size)
+ * ([dense] _segmented_mla_page_size); the sparse variant has no page
+ * structure and uses a 64-entry tile.
+ * Errors: MLA_ERR_INVALID_ARG for NULL pointers or inconsistent sizes,
+ * MLA_ERR_UNSUPPORTED for head_dim != 576, kv_lora_rank != 512,
+ * num_heads > 128, q_dtype != kv_dtype, or topk not a multiple of 128.
+ */
+MLA_API mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan);
+
+/*
+ * mla_decode_fwd -- the whole decode: split-K segments, then the merge
+ * (skipped when NS == 1: the segment kernel then writes out and lse itself).
+ *
+ *   q            [T, H, 576] in q_dtype ([dense] forward_mqa: ql_nope || q_pe)
+ *   kv_cache     [num_blocks, block_size, 576] in kv_dtype
+ *   block_table  [R, >= max_blocks_per_req] int32, row stride
+ *                block_table_stride elements (dense; may be NULL if sparse)
+ *   seq_lens     [R] int32 KV length of each request including its new
+ *                tokens (dense; may be NULL if sparse)
+ *   qo_indptr    [R + 1] int32 token offsets of the requests, or NULL for one
+ *                token per request. Row j of a qlen-token request sees
+ *                positions [0, seq_len - qlen + j] ([dense]
+ *                dcp_local_verify_row_lens).
+ *   sparse_slots global cache slots (output of mla_sparse_index_convert),
+ *                -1 = unused entry; [T, topk] when sparse_indptr is NULL,
+ *                else a flat list where token t owns
+ *                [sparse_indptr[t], sparse_indptr[t + 1]) (at most topk).
+ *                NULL for the dense variant. Mutually exclusive with qo_indptr.
+ *   softmax_scale, q_scale, kv_scale: score = softmax_scale * q_scale *
+ *                kv_scale * (q . k) over 576 columns; values are scaled by
+ *                kv_scale. Scales are 1 for bf16.
+ *   sinks        [H] fp32 natural-log sink logits or NULL ([sparse]
+ *                _forward_mla): a sink adds e^sink to the softmax denominator
+ *                and nothing to the output.
+ *   workspace    plan->workspace_bytes of device memory (NULL allowed when
+ *                that is 0); contents need not be initialised.
+ *   out          [T, H, 512] bf16; lse [T, H] fp32 natural log. Every element
+ *                is written; a row with no visible key gets out = 0 and
+ *                lse = -inf (or its sink).
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_WORKSPACE, MLA_ERR_CUDA.
+ */
+MLA_API mla_status_t mla_decode_fwd(const mla_plan_t* plan, const void* q, const void* kv_cache,
+                            const int32_t* block_table, int64_t block_table_stride,
+                            const int32_t* seq_lens, const int32_t* qo_indptr,
+                            const int32_t* sparse_slots, const int32_t* sparse_indptr,
+                            float softmax_scale, float q_scale, float kv_scale,
+                            const float* sinks, void* workspace, size_t workspace_bytes,
+                            void* out, float* lse, cudaStream_t stream);
+
+/*
+ * mla_decode_segments -- the split-K stage alone: base-2 partials of every
+ * segment ([merge] module docstring, "each segment emits base-2 partials").
+ * Same inputs as mla_decode_fwd; sinks are not used here (the merge folds
+ * them). For segment s of token t, head h, over the keys of the segment the
+ * row may see, with s2 = score * log2(e):
+ *   segm_max   [T, H, NS]      m2 = max s2          (-inf if no key)
+ *   segm_expsum[T, H, NS]      l  = sum 2^(s2 - m2) (0 if no key)
+ *   segm_output[T, H, NS, 512] o  = sum 2^(s2 - m2) v / l (0 if no key)
+ * The partition of token t is [s*tps*tile, min((s+1)*tps*tile, len)) with
+ * tps = cdiv(len, NS * tile), len = seq_len of its request (shared by all
+ * rows of a multi-token request) or the length of its slot list.
+ * Every element of the three arrays is written, empty segments included.
+ */
+MLA_API mla_status_t mla_decode_segments(const mla_plan_t* plan, const void* q, const void* kv_cache,
+                                 const int32_t* block_table, int64_t block_table_stride,
+                                 const int32_t* seq_lens, const int32_t* qo_indptr,
+                                 const int32_t* sparse_slots, const int32_t* sparse_indptr,
+                                 float softmax_scale, float q_scale, float kv_scale,
+                                 float* segm_output, float* segm_max, float* segm_expsum,
+                                 cudaStream_t stream);
+
+/*
+ * mla_merge_segments -- merge base-2 partials into out and natural-log lse
+ * ([merge] merge_mla_segments_triton). For token t the segments whose start
+ * lies inside [0, part_lens[t]) (partition as above, from part_lens and
+ * tile_size) and whose expsum is > 0 take part. With M = max(m2_s,
+ * sink * log2 e) and W = sum_s l_s 2^(m2_s - M) + 2^(sink log2 e - M):
+ *   out = sum_s l_s 2^(m2_s - M) o_s / W,   lse = ln 2 * (M + log2 W).
+ * No contributing segment and no sink: out = 0, lse = -inf.
+ *   segm_output [T, H, NS, kv_lora_rank] fp32, segm_max / segm_expsum
+ *   [T, H, NS] fp32, part_lens [T] int32, sinks [H] fp32 or NULL,
+ *   out [T, H, kv_lora_rank] in out_dtype (BF16 only), lse [T, H] fp32.
+ * kv_lora_rank must be a positive multiple of 128; num_segments 1..64.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_UNSUPPORTED (out_dtype), MLA_ERR_CUDA.
+ */
+MLA_API mla_status_t mla_merge_segments(const float* segm_output, const float* segm_max,
+                                const float* segm_expsum, const int32_t* part_lens,
+                                int32_t num_tokens, int32_t num_heads, int32_t num_segments,
+                                int32_t kv_lora_rank, int32_t tile_size, const float* sinks,
+                                int32_t out_dtype, void* out, float* lse, cudaStream_t stream);
+
+/*
+ * mla_sparse_index_convert -- per-request top-k positions to global slots
+ * ([sparse] triton_convert_req_index_to_global_index):
+ *   out[t, i] = block_table[req_id[t], idx / block_size] * block_size
+ *               + idx % block_size,   idx = token_indices[t, i],
+ * and -1 when idx < 0, when idx / block_size >= bt_cols, or when req_id[t]
+ * is not in [0, bt_rows). Block-table values are not range-checked.
+ * Integer arithmetic in int32; the caller keeps num_blocks * block_size
+ * below 2^31.
+ *   req_id        [T] int32
+ *   block_table   [bt_rows, bt_cols] int32 with row stride bt_row_stride
+ *   token_indices [T, topk] int32 with row stride ti_row_stride
+ *   cu_seqlens    NULL: out is [T, topk]. Else [T + 1] int32 and the first
+ *                 cu_seqlens[t+1] - cu_seqlens[t] (<= topk) entries of row t
+ *                 are written to out[cu_seqlens[t] + i]; nothing else in out
+ *                 is touched.
+ * topk must be a positive multiple of 128; block_size > 0.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_CUDA.
+ */
+MLA_API mla_status_t mla_sparse_index_convert(const int32_t* req_id, const int32_t* block_table,
+                                      int32_t bt_rows, int32_t bt_cols, int64_t bt_row_stride,
+                                      const int32_t* token_indices, int64_t ti_row_stride,
+                                      int32_t num_tokens, int32_t topk, int32_t block_size,
+                                      const int32_t* cu_seqlens, int32_t* out,
+                                      cudaStream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+MLA_API const char* mla_status_string(mla_status_t status);
+
+/* CUDA error string recorded by the last MLA_ERR_CUDA on the calling thread,
+ * or "" (static / thread-local storage). */
+MLA_API const char* mla_last_cuda_error(void);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+MLA_API int32_t mla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_DECODE_H_ */

@@ -1,0 +1,375 @@
+// api.cu -- the C ABI declared in include/mla_decode.h: host-side argument
+// checks, the planner, and the launches of the decode, merge and index
+// kernels. Nothing here allocates device memory or synchronises a stream.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+#include "internal.h"
+#include "mla_decode.h"
+
+namespace {
+
+constexpr int kHeadDim = 576;
+constexpr int kRank = 512;
+constexpr int kMaxHeads = 128;
+constexpr int kMaxSegments = 64;
+constexpr int kSparseTile = 64;
+constexpr size_t kWsAlign = 256;
+
+thread_local const char* g_last_cuda_error = "";
+
+mla_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MLA_OK;
+  g_last_cuda_error = cudaGetErrorString(e);
+  return MLA_ERR_CUDA;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Largest power of two dividing the block, capped at 128
+// (rocm_aiter_mla.py, _segmented_mla_page_size).
+int32_t tile_for_block(int32_t bs) {
+  const int32_t low = bs & -bs;
+  return low < 128 ? low : 128;
+}
+
+mla_status_t check_problem(const mla_problem_t& p) {
+  if (p.num_tokens < 0 || p.num_heads <= 0 || p.block_size <= 0) return MLA_ERR_INVALID_ARG;
+  if (p.head_dim != kHeadDim || p.kv_lora_rank != kRank) return MLA_ERR_UNSUPPORTED;
+  if (p.num_heads > kMaxHeads) return MLA_ERR_UNSUPPORTED;
+  if (p.q_dtype != MLA_DTYPE_BF16 && p.q_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (p.kv_dtype != MLA_DTYPE_BF16 && p.kv_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (p.q_dtype != p.kv_dtype) return MLA_ERR_UNSUPPORTED;
+  if (p.num_blocks <= 0) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(p.num_blocks) * p.block_size > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (p.num_segments < 0 || p.num_segments > kMaxSegments) return MLA_ERR_INVALID_ARG;
+  if (p.num_sms < 0 || p.has_sinks < 0 || p.has_sinks > 1) return MLA_ERR_INVALID_ARG;
+  if (p.topk < 0) return MLA_ERR_INVALID_ARG;
+  if (p.topk > 0) {
+    if (p.topk % 128 != 0) return MLA_ERR_UNSUPPORTED;
+    if (p.max_qlen > 1) return MLA_ERR_INVALID_ARG;  // sparse rows are single tokens
+    if (p.num_tokens > 65535) return MLA_ERR_UNSUPPORTED;
+  } else {
+    if (p.num_reqs < 0 || p.max_blocks_per_req <= 0) return MLA_ERR_INVALID_ARG;
+    if (p.max_seq_len < 0 || p.max_qlen < 1) return MLA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(p.max_seq_len) > static_cast<int64_t>(p.max_blocks_per_req) * p.block_size)
+      return MLA_ERR_INVALID_ARG;
+    if (p.num_reqs > 65535) return MLA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(p.max_qlen) * p.num_heads > (1 << 20)) return MLA_ERR_UNSUPPORTED;
+  }
+  return MLA_OK;
+}
+
+struct Inputs {
+  const void* q;
+  const void* kv;
+  const int32_t* bt;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  const int32_t* qo_indptr;
+  const int32_t* slots;
+  const int32_t* slot_indptr;
+  float softmax_scale, q_scale, kv_scale;
+};
+
+mla_status_t check_inputs(const mla_plan_t* plan, const Inputs& in) {
+  if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  const mla_problem_t& p = plan->prob;
+  mla_status_t s = check_problem(p);
+  if (s != MLA_OK) return s;
+  if (plan->num_segments < 1 || plan->num_segments > kMaxSegments || plan->tile_size <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (p.num_tokens == 0) return MLA_OK;
+  if (in.q == nullptr || in.kv == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned(in.q, 16) || !aligned(in.kv, 16)) return MLA_ERR_INVALID_ARG;
+  if (!std::isfinite(in.softmax_scale) || !std::isfinite(in.q_scale) || !std::isfinite(in.kv_scale) ||
+      !(in.q_scale > 0.f) || !(in.kv_scale > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (p.topk > 0) {
+    if (in.slots == nullptr || in.qo_indptr != nullptr) return MLA_ERR_INVALID_ARG;
+    if (!aligned(in.slots, 4)) return MLA_ERR_INVALID_ARG;
+  } else {
+    if (in.bt == nullptr || in.seq_lens == nullptr || in.slots != nullptr) return MLA_ERR_INVALID_ARG;
+    if (in.bt_stride < p.max_blocks_per_req) return MLA_ERR_INVALID_ARG;
+    if (p.max_qlen > 1 && in.qo_indptr == nullptr) return MLA_ERR_INVALID_ARG;
+    if (in.qo_indptr == nullptr && p.num_tokens != p.num_reqs) return MLA_ERR_INVALID_ARG;
+    if (!aligned(in.bt, 4) || !aligned(in.seq_lens, 4)) return MLA_ERR_INVALID_ARG;
+  }
+  return MLA_OK;
+}
+
+mla::DecodeParams make_params(const mla_plan_t* plan, const Inputs& in) {
+  const mla_problem_t& p = plan->prob;
+  mla::DecodeParams d{};
+  d.q = in.q;
+  d.kv = in.kv;
+  d.block_table = in.bt;
+  d.bt_stride = in.bt_stride;
+  d.seq_lens = in.seq_lens;
+  d.qo_indptr = in.qo_indptr;
+  d.slots = p.topk > 0 ? in.slots : nullptr;
+  d.slot_indptr = p.topk > 0 ? in.slot_indptr : nullptr;
+  d.num_tokens = p.num_tokens;
+  d.num_reqs = p.num_reqs;
+  d.num_heads = p.num_heads;
+  d.block_size = p.block_size;
+  d.topk = p.topk;
+  d.num_segments = plan->num_segments;
+  d.tile_size = plan->tile_size;
+  d.row_tiles = plan->row_tiles;
+  d.score_scale_log2 = in.softmax_scale * in.q_scale * in.kv_scale * 1.4426950408889634f;
+  d.kv_scale = in.kv_scale;
+  return d;
+}
+
+mla::PartLens part_lens_for(const mla_plan_t* plan, const Inputs& in) {
+  const mla_problem_t& p = plan->prob;
+  mla::PartLens pl{};
+  if (p.topk > 0) {
+    if (in.slot_indptr != nullptr) {
+      pl.mode = 2;
+      pl.indptr = in.slot_indptr;
+    } else {
+      pl.mode = 3;
+      pl.constant = p.topk;
+    }
+  } else {
+    pl.mode = 1;
+    pl.seq_lens = in.seq_lens;
+    pl.qo_indptr = in.qo_indptr;
+    pl.num_reqs = p.num_reqs;
+  }
+  return pl;
+}
+
+dim3 grid_of(const mla_plan_t* plan) {
+  return dim3(static_cast<unsigned>(plan->grid_x), static_cast<unsigned>(plan->grid_y),
+              static_cast<unsigned>(plan->grid_z));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mla_status_string(mla_status_t s) {
+  switch (s) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    default: return "MLA_ERR_UNKNOWN";
+  }
+}
+
+const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
+
+int32_t mla_version(void) { return 100; }
+
+mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
+  if (prob == nullptr || plan == nullptr) return MLA_ERR_INVALID_ARG;
+  const mla_problem_t p = *prob;
+  mla_status_t s = check_problem(p);
+  if (s != MLA_OK) return s;
+  std::memset(plan, 0, sizeof(*plan));
+  plan->prob = p;
+
+  int32_t sms = p.num_sms;
+  if (sms == 0) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
+  plan->num_sms = sms;
+
+  const bool sparse = p.topk > 0;
+  const int32_t units = sparse ? p.num_tokens : p.num_reqs;
+  const int64_t rows_per_unit = sparse ? p.num_heads : static_cast<int64_t>(p.num_heads) * p.max_qlen;
+  int32_t kernel, rows;
+  if (rows_per_unit <= 16) {
+    kernel = mla::kMmaRows16;
+    rows = 16;
+  } else if (rows_per_unit <= 32) {
+    kernel = mla::kMmaRows32;
+    rows = 32;
+  } else {
+    kernel = mla::kMmaRows64;
+    rows = 64;
+  }
+  const int32_t row_tiles = static_cast<int32_t>((rows_per_unit + rows - 1) / rows);
+  const int32_t tile = sparse ? kSparseTile : tile_for_block(p.block_size);
+  const int32_t max_len = sparse ? p.topk : p.max_seq_len;
+
+  int32_t ns = p.num_segments;
+  if (ns == 0) {
+    // Enough CTAs for about two per SM, but no segment shorter than
+    // ~512 keys: each extra segment costs a partial write and read.
+    const int64_t per_seg = static_cast<int64_t>(units > 0 ? units : 1) * row_tiles;
+    int64_t want = (2 * static_cast<int64_t>(sms) + per_seg - 1) / per_seg;
+    const int64_t cap = max_len / 512 > 1 ? max_len / 512 : 1;
+    if (want > cap) want = cap;
+    if (want > 16) want = 16;
+    ns = static_cast<int32_t>(want < 1 ? 1 : want);
+  }
+
+  plan->num_segments = ns;
+  plan->tile_size = tile;
+  plan->kernel = kernel;
+  plan->rows_per_cta = rows;
+  plan->row_tiles = row_tiles;
+  plan->grid_x = row_tiles;
+  plan->grid_y = ns;
+  plan->grid_z = units;
+  if (ns > 1) {
+    const size_t th = static_cast<size_t>(p.num_tokens) * p.num_heads;
+    const size_t out_b = align_up(th * ns * kRank * sizeof(float), kWsAlign);
+    const size_t max_b = align_up(th * ns * sizeof(float), kWsAlign);
+    plan->segm_max_offset = out_b;
+    plan->segm_expsum_offset = out_b + max_b;
+    plan->workspace_bytes = out_b + 2 * max_b;
+  }
+  return MLA_OK;
+}
+
+mla_status_t mla_decode_segments(const mla_plan_t* plan, const void* q, const void* kv_cache,
+                                 const int32_t* block_table, int64_t block_table_stride,
+                                 const int32_t* seq_lens, const int32_t* qo_indptr,
+                                 const int32_t* sparse_slots, const int32_t* sparse_indptr,
+                                 float softmax_scale, float q_scale, float kv_scale,
+                                 float* segm_output, float* segm_max, float* segm_expsum,
+                                 cudaStream_t stream) {
+  const Inputs in{q, kv_cache, block_table, block_table_stride, seq_lens, qo_indptr,
+                  sparse_slots, sparse_indptr, softmax_scale, q_scale, kv_scale};
+  mla_status_t s = check_inputs(plan, in);
+  if (s != MLA_OK) return s;
+  if (plan->prob.num_tokens == 0) return MLA_OK;
+  if (segm_output == nullptr || segm_max == nullptr || segm_expsum == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(segm_output, 16) || !aligned(segm_max, 4) || !aligned(segm_expsum, 4))
+    return MLA_ERR_INVALID_ARG;
+  mla::DecodeParams d = make_params(plan, in);
+  d.final_mode = 0;
+  d.segm_out = segm_output;
+  d.segm_max = segm_max;
+  d.segm_expsum = segm_expsum;
+  if (plan->grid_z == 0) return MLA_OK;
+  return cuda_status(mla::launch_decode_mma(plan->kernel, plan->prob.kv_dtype == MLA_DTYPE_FP8_E4M3,
+                                            d, grid_of(plan), stream));
+}
+
+mla_status_t mla_decode_fwd(const mla_plan_t* plan, const void* q, const void* kv_cache,
+                            const int32_t* block_table, int64_t block_table_stride,
+                            const int32_t* seq_lens, const int32_t* qo_indptr,
+                            const int32_t* sparse_slots, const int32_t* sparse_indptr,
+                            float softmax_scale, float q_scale, float kv_scale,
+                            const float* sinks, void* workspace, size_t workspace_bytes,
+                            void* out, float* lse, cudaStream_t stream) {
+  const Inputs in{q, kv_cache, block_table, block_table_stride, seq_lens, qo_indptr,
+                  sparse_slots, sparse_indptr, softmax_scale, q_scale, kv_scale};
+  mla_status_t s = check_inputs(plan, in);
+  if (s != MLA_OK) return s;
+  const mla_problem_t& p = plan->prob;
+  if ((sinks != nullptr) != (p.has_sinks == 1)) return MLA_ERR_INVALID_ARG;
+  if (p.num_tokens == 0) return MLA_OK;
+  if (out == nullptr || lse == nullptr || !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (sinks != nullptr && !aligned(sinks, 4)) return MLA_ERR_INVALID_ARG;
+  if (plan->workspace_bytes > 0) {
+    if (workspace == nullptr || workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE;
+    if (!aligned(workspace, kWsAlign)) return MLA_ERR_INVALID_ARG;
+  }
+  mla::DecodeParams d = make_params(plan, in);
+  const bool fp8 = p.kv_dtype == MLA_DTYPE_FP8_E4M3;
+  if (plan->num_segments == 1) {
+    d.final_mode = 1;
+    d.sinks = sinks;
+    d.out = out;
+    d.lse = lse;
+    if (plan->grid_z == 0) return MLA_OK;
+    return cuda_status(mla::launch_decode_mma(plan->kernel, fp8, d, grid_of(plan), stream));
+  }
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  d.final_mode = 0;
+  d.segm_out = reinterpret_cast<float*>(ws);
+  d.segm_max = reinterpret_cast<float*>(ws + plan->segm_max_offset);
+  d.segm_expsum = reinterpret_cast<float*>(ws + plan->segm_expsum_offset);
+  if (plan->grid_z > 0) {
+    s = cuda_status(mla::launch_decode_mma(plan->kernel, fp8, d, grid_of(plan), stream));
+    if (s != MLA_OK) return s;
+  }
+  mla::MergeParams m{};
+  m.segm_out = d.segm_out;
+  m.segm_max = d.segm_max;
+  m.segm_expsum = d.segm_expsum;
+  m.part = part_lens_for(plan, in);
+  m.num_tokens = p.num_tokens;
+  m.num_heads = p.num_heads;
+  m.num_segments = plan->num_segments;
+  m.rank = kRank;
+  m.tile_size = plan->tile_size;
+  m.sinks = sinks;
+  m.out = out;
+  m.lse = lse;
+  return cuda_status(mla::launch_merge(m, stream));
+}
+
+mla_status_t mla_merge_segments(const float* segm_output, const float* segm_max,
+                                const float* segm_expsum, const int32_t* part_lens,
+                                int32_t num_tokens, int32_t num_heads, int32_t num_segments,
+                                int32_t kv_lora_rank, int32_t tile_size, const float* sinks,
+                                int32_t out_dtype, void* out, float* lse, cudaStream_t stream) {
+  if (num_tokens < 0 || num_heads <= 0 || num_segments < 1 || num_segments > kMaxSegments ||
+      tile_size <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (kv_lora_rank != 128 && kv_lora_rank != 256 && kv_lora_rank != 512) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_DTYPE_BF16) return MLA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return MLA_OK;
+  if (segm_output == nullptr || segm_max == nullptr || segm_expsum == nullptr ||
+      part_lens == nullptr || out == nullptr || lse == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(segm_output, 16) || !aligned(out, 16) || !aligned(lse, 4) ||
+      !aligned(segm_max, 4) || !aligned(segm_expsum, 4) || !aligned(part_lens, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (sinks != nullptr && !aligned(sinks, 4)) return MLA_ERR_INVALID_ARG;
+  mla::MergeParams m{};
+  m.segm_out = segm_output;
+  m.segm_max = segm_max;
+  m.segm_expsum = segm_expsum;
+  m.part.mode = 0;
+  m.part.lens = part_lens;
+  m.num_tokens = num_tokens;
+  m.num_heads = num_heads;
+  m.num_segments = num_segments;
+  m.rank = kv_lora_rank;
+  m.tile_size = tile_size;
+  m.sinks = sinks;
+  m.out = out;
+  m.lse = lse;
+  return cuda_status(mla::launch_merge(m, stream));
+}
+
+mla_status_t mla_sparse_index_convert(const int32_t* req_id, const int32_t* block_table,
+                                      int32_t bt_rows, int32_t bt_cols, int64_t bt_row_stride,
+                                      const int32_t* token_indices, int64_t ti_row_stride,
+                                      int32_t num_tokens, int32_t topk, int32_t block_size,
+                                      const int32_t* cu_seqlens, int32_t* out,
+                                      cudaStream_t stream) {
+  if (num_tokens < 0 || topk <= 0 || topk % 128 != 0 || block_size <= 0) return MLA_ERR_INVALID_ARG;
+  if (bt_rows <= 0 || bt_cols <= 0 || bt_row_stride < bt_cols || ti_row_stride < topk)
+    return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_tokens) * (topk / 128) > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return MLA_OK;
+  if (req_id == nullptr || block_table == nullptr || token_indices == nullptr || out == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(req_id, 4) || !aligned(block_table, 4) || !aligned(token_indices, 4) ||
+      !aligned(out, 4) || (cu_seqlens != nullptr && !aligned(cu_seqlens, 4)))
+    return MLA_ERR_INVALID_ARG;
+  return cuda_status(mla::launch_index_convert(req_id, block_table, bt_rows, bt_cols, bt_row_stride,
+                                               token_indices, ti_row_stride, num_tokens, topk,
+                                               block_size, cu_seqlens, out, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// internal.h -- parameter blocks and launchers shared between the C ABI
+// layer (api.cu) and the kernels. Not part of the public interface.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime_api.h>
+
+namespace mla {
+
+// Decode kernel variants chosen by the planner.
+enum KernelId : int32_t {
+  kMmaRows16 = 1,   // warp-MMA split-K kernel, 16 query rows per CTA
+  kMmaRows32 = 2,   // 32 rows per CTA
+  kMmaRows64 = 3,   // 64 rows per CTA
+};
+
+struct DecodeParams {
+  const void* q;                 // [T, H, 576]
+  const void* kv;                // [NB, BS, 576]
+  const int32_t* block_table;    // dense
+  int64_t bt_stride;
+  const int32_t* seq_lens;       // dense [R]
+  const int32_t* qo_indptr;      // dense [R+1] or null
+  const int32_t* slots;          // sparse slot list or null
+  const int32_t* slot_indptr;    // sparse [T+1] or null ([T, topk] layout)
+  int32_t num_tokens, num_reqs, num_heads, block_size, topk;
+  int32_t num_segments, tile_size, row_tiles;
+  float score_scale_log2;        // softmax_scale * q_scale * kv_scale * log2(e)
+  float kv_scale;
+  const float* sinks;            // [H] or null (final mode only)
+  int32_t final_mode;            // 1: write out/lse; 0: write segment partials
+  float* segm_out;               // [T, H, NS, 512]
+  float* segm_max;               // [T, H, NS]
+  float* segm_expsum;            // [T, H, NS]
+  void* out;                     // [T, H, 512] bf16
+  float* lse;                    // [T, H]
+};
+
+// Where the merge finds each token's partition length.
+struct PartLens {
+  const int32_t* lens;       // mode 0: lens[t]
+  const int32_t* seq_lens;   // mode 1: seq_lens[request of t] via qo_indptr
+  const int32_t* qo_indptr;
+  const int32_t* indptr;     // mode 2: indptr[t+1] - indptr[t]
+  int32_t num_reqs;
+  int32_t constant;          // mode 3: constant
+  int32_t mode;
+};
+
+struct MergeParams {
+  const float* segm_out;
+  const float* segm_max;
+  const float* segm_expsum;
+  PartLens part;
+  int32_t num_tokens, num_heads, num_segments, rank, tile_size;
+  const float* sinks;
+  void* out;     // bf16
+  float* lse;
+};
+
+cudaError_t launch_decode_mma(int32_t kernel, bool fp8, const DecodeParams& p, dim3 grid,
+                              cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_index_convert(const int32_t* req_id, const int32_t* block_table,
+                                 int32_t bt_rows, int32_t bt_cols, int64_t bt_stride,
+                                 const int32_t* token_indices, int64_t ti_stride,
+                                 int32_t num_tokens, int32_t topk, int32_t block_size,
+                                 const int32_t* cu_seqlens, int32_t* out, cudaStream_t stream);
+
+// Shared memory bytes a decode variant needs (host query for validation).
+int decode_mma_smem_bytes(int32_t kernel, bool fp8);
+
+}  // namespace mla

@@ -1,0 +1,207 @@
+"""Host-side checks of the C ABI: the library loads, exports every entry point
+declared in include/*.h, plans problems, and rejects bad arguments with the
+documented status before launching anything. No GPU needed: every call here
+either stays on the host or fails validation before a launch.
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from paged_mla_decode_06_gb300 import binding as B
+from paged_mla_decode_06_gb300 import build as BUILD
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    BUILD.build()
+    return B.load_library()
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        names.update(re.findall(r"MLA_API\s+[\w\s\*]+?\b(mla_\w+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_symbols()
+    assert {"mla_decode_plan", "mla_decode_fwd", "mla_decode_segments", "mla_merge_segments",
+            "mla_sparse_index_convert"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_struct_sizes_match_the_header(lib):
+    assert ctypes.sizeof(B.Problem) == 16 * 4
+    # 16 problem ints + 9 plan ints + 4 reserved (+ pad) + 3 size_t
+    assert ctypes.sizeof(B.Plan) == 144
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "MLA_OK"), (1, "MLA_ERR_INVALID_ARG"), (2, "MLA_ERR_UNSUPPORTED"),
+                       (3, "MLA_ERR_WORKSPACE"), (4, "MLA_ERR_CUDA")]:
+        assert lib.mla_status_string(code).decode() == name
+    assert lib.mla_version() >= 100
+
+
+def _dense_problem(**kw):
+    base = dict(num_tokens=64, num_reqs=64, num_heads=128, block_size=64, num_blocks=5000,
+                max_blocks_per_req=130, max_seq_len=8192, num_sms=152)
+    base.update(kw)
+    return B.make_problem(**base)
+
+
+def test_plan_dense_defaults(lib):
+    plan = B.mla_decode_plan(_dense_problem())
+    assert plan.tile_size == 64
+    assert plan.rows_per_cta == 64 and plan.row_tiles == 2
+    assert plan.grid_x == 2 and plan.grid_z == 64 and plan.grid_y == plan.num_segments
+    assert 1 <= plan.num_segments <= 16
+    if plan.num_segments > 1:
+        th = 64 * 128
+        assert plan.workspace_bytes >= th * plan.num_segments * (512 + 2) * 4
+        assert plan.segm_max_offset % 256 == 0 and plan.segm_expsum_offset % 256 == 0
+
+
+def test_plan_tile_rule_golden(lib):
+    rows = [l.split() for l in open(os.path.join(ROOT, "tests", "golden", "tile_rule.txt"))
+            if l.strip() and not l.startswith("#")]
+    for bs, tile in rows:
+        bs = int(bs)
+        plan = B.mla_decode_plan(_dense_problem(block_size=bs, max_blocks_per_req=9000,
+                                                max_seq_len=8192, num_blocks=10000))
+        assert plan.tile_size == int(tile), bs
+
+
+def test_plan_explicit_segments_and_small_heads(lib):
+    plan = B.mla_decode_plan(_dense_problem(num_heads=16, num_segments=4, num_tokens=2,
+                                            num_reqs=2, block_size=16, max_seq_len=130,
+                                            max_blocks_per_req=10))
+    assert plan.num_segments == 4 and plan.tile_size == 16
+    assert plan.rows_per_cta == 16 and plan.row_tiles == 1
+
+
+def test_plan_multi_token_rows(lib):
+    plan = B.mla_decode_plan(_dense_problem(num_tokens=96, num_reqs=32, max_qlen=4,
+                                            max_seq_len=8192))
+    assert plan.row_tiles == 8  # 4 tokens x 128 heads / 64 rows
+
+
+def test_plan_sparse(lib):
+    plan = B.mla_decode_plan(B.make_problem(num_tokens=128, num_heads=128, block_size=64,
+                                            num_blocks=16384, topk=2048, num_sms=152))
+    assert plan.tile_size == 64 and plan.grid_z == 128
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim_override=512), B.MLA_ERR_UNSUPPORTED),
+    (dict(num_heads=129), B.MLA_ERR_UNSUPPORTED),
+    (dict(num_heads=0), B.MLA_ERR_INVALID_ARG),
+    (dict(block_size=0), B.MLA_ERR_INVALID_ARG),
+    (dict(num_segments=65), B.MLA_ERR_INVALID_ARG),
+    (dict(topk=100, num_reqs=0), B.MLA_ERR_UNSUPPORTED),
+    (dict(max_seq_len=100000), B.MLA_ERR_INVALID_ARG),
+    (dict(max_qlen=0), B.MLA_ERR_INVALID_ARG),
+    (dict(mixed_dtype=True), B.MLA_ERR_UNSUPPORTED),
+])
+def test_plan_rejects(lib, kw, status):
+    kw = dict(kw)
+    hd = kw.pop("head_dim_override", None)
+    mixed = kw.pop("mixed_dtype", False)
+    prob = _dense_problem(**kw)
+    if hd is not None:
+        prob.head_dim = hd
+    if mixed:
+        prob.kv_dtype = B.MLA_DTYPE_FP8_E4M3
+    plan = B.Plan()
+    assert lib.mla_decode_plan(ctypes.byref(prob), ctypes.byref(plan)) == status
+    assert lib.mla_decode_plan(None, ctypes.byref(plan)) == B.MLA_ERR_INVALID_ARG
+
+
+FAKE = 0x10000  # aligned, never dereferenced: every call below fails validation first
+
+
+def _fwd(lib, plan, **over):
+    args = dict(q=FAKE, kv=FAKE, bt=FAKE, bts=130, seq=FAKE, qo=None, slots=None, sind=None,
+                sc=0.07, qs=1.0, ks=1.0, sinks=None, ws=FAKE, wsb=1 << 40, out=FAKE, lse=FAKE)
+    args.update(over)
+    return lib.mla_decode_fwd(ctypes.byref(plan), args["q"], args["kv"], args["bt"], args["bts"],
+                              args["seq"], args["qo"], args["slots"], args["sind"], args["sc"],
+                              args["qs"], args["ks"], args["sinks"], args["ws"], args["wsb"],
+                              args["out"], args["lse"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(q=None), B.MLA_ERR_INVALID_ARG),
+    (dict(kv=FAKE + 8), B.MLA_ERR_INVALID_ARG),          # misaligned cache
+    (dict(bt=None), B.MLA_ERR_INVALID_ARG),
+    (dict(bts=10), B.MLA_ERR_INVALID_ARG),               # stride < max_blocks_per_req
+    (dict(seq=None), B.MLA_ERR_INVALID_ARG),
+    (dict(slots=FAKE), B.MLA_ERR_INVALID_ARG),           # sparse list on a dense plan
+    (dict(sinks=FAKE), B.MLA_ERR_INVALID_ARG),           # sinks not announced in the problem
+    (dict(out=None), B.MLA_ERR_INVALID_ARG),
+    (dict(lse=FAKE + 2), B.MLA_ERR_INVALID_ARG),
+    (dict(qs=0.0), B.MLA_ERR_INVALID_ARG),
+    (dict(sc=float("nan")), B.MLA_ERR_INVALID_ARG),
+])
+def test_fwd_rejects_bad_arguments(lib, over, status):
+    plan = B.mla_decode_plan(_dense_problem(num_segments=1))
+    assert _fwd(lib, plan, **over) == status
+
+
+def test_fwd_rejects_small_workspace(lib):
+    plan = B.mla_decode_plan(_dense_problem(num_segments=4))
+    assert plan.workspace_bytes > 0
+    assert _fwd(lib, plan, wsb=plan.workspace_bytes - 1) == B.MLA_ERR_WORKSPACE
+    assert _fwd(lib, plan, ws=None) == B.MLA_ERR_WORKSPACE
+    assert _fwd(lib, plan, ws=FAKE + 128) == B.MLA_ERR_INVALID_ARG
+
+
+def test_fwd_requires_qo_indptr_for_multi_token(lib):
+    plan = B.mla_decode_plan(_dense_problem(num_tokens=96, num_reqs=32, max_qlen=4,
+                                            num_segments=1))
+    assert _fwd(lib, plan) == B.MLA_ERR_INVALID_ARG
+
+
+def test_fwd_sparse_rejects_qo_indptr(lib):
+    plan = B.mla_decode_plan(B.make_problem(num_tokens=128, num_heads=128, block_size=64,
+                                            num_blocks=16384, topk=2048, num_sms=152,
+                                            num_segments=1))
+    assert _fwd(lib, plan, slots=FAKE, qo=FAKE) == B.MLA_ERR_INVALID_ARG
+    assert _fwd(lib, plan, slots=None) == B.MLA_ERR_INVALID_ARG
+
+
+def test_merge_rejects(lib):
+    f = lib.mla_merge_segments
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 0, 512, 16, None, 0, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 500, 16, None, 0, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, FAKE, FAKE, 4, 8, 2, 512, 16, None, 1, FAKE, FAKE, None) == B.MLA_ERR_UNSUPPORTED
+    assert f(None, FAKE, FAKE, FAKE, 4, 8, 2, 512, 16, None, 0, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE + 4, FAKE, FAKE, FAKE, 4, 8, 2, 512, 16, None, 0, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    # zero tokens: nothing to do, nothing launched
+    assert f(None, None, None, None, 0, 8, 2, 512, 16, None, 0, None, None, None) == B.MLA_OK
+
+
+def test_index_convert_rejects(lib):
+    f = lib.mla_sparse_index_convert
+    assert f(FAKE, FAKE, 4, 8, 8, FAKE, 2048, 16, 2000, 64, None, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 8, 8, FAKE, 2048, 16, 2048, 0, None, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 8, 4, FAKE, 2048, 16, 2048, 64, None, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 4, 8, 8, FAKE, 1024, 16, 2048, 64, None, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(None, FAKE, 4, 8, 8, FAKE, 2048, 16, 2048, 64, None, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE + 1, FAKE, 4, 8, 8, FAKE, 2048, 16, 2048, 64, None, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(None, None, 4, 8, 8, None, 2048, 0, 2048, 64, None, None, None) == B.MLA_OK
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="not found"):
+        B.load_library(str(tmp_path / "nope.so"))

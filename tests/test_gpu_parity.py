@@ -1,0 +1,336 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Small cases are compared element by element on every token; the full-size
+workloads, in the launch configuration the benchmark times, are compared on
+sampled tokens the oracle computes one by one. Tolerances: bf16 output
+max-abs 1e-2, fp8 output 2e-2, LSE 1e-3 absolute, index conversion
+bit-exact. Caches carry NaN in every slot the decode must not read.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from paged_mla_decode_06_gb300 import binding as B
+from paged_mla_decode_06_gb300 import build as BUILD
+from paged_mla_decode_06_gb300 import inputs as I
+from tests.gpu_helpers import assert_close, oracle_slots, run_gpu, run_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    BUILD.build()
+    B.load_library()
+
+
+# ---------------------------------------------------------------- index conversion
+
+def _convert_case(seed, T, topk, rows, cols, bs):
+    rng = np.random.default_rng(seed)
+    bt = rng.integers(0, 1 << 14, size=(rows, cols)).astype(np.int32)
+    req = rng.integers(0, rows, size=T).astype(np.int32)
+    ti = rng.integers(-2, cols * bs + 3 * bs, size=(T, topk)).astype(np.int32)
+    ti[:, -1] = cols * bs - 1       # last valid position
+    ti[0, :8] = -1
+    if T > 2:
+        req[2] = rows                # request outside the table
+        req[1] = -1
+    return req, bt, ti
+
+
+@pytest.mark.parametrize("T,topk,rows,cols,bs", [
+    (5, 128, 3, 7, 16), (33, 256, 9, 40, 64), (128, 2048, 16, 1024, 64), (7, 384, 4, 13, 48)])
+def test_index_convert_bit_exact(T, topk, rows, cols, bs):
+    req, bt, ti = _convert_case(T + topk, T, topk, rows, cols, bs)
+    want = O.index_convert(req, bt, ti, bs)
+    dev = torch.device("cuda")
+    out = torch.full((T, topk), 7, dtype=torch.int32, device=dev)
+    B.mla_sparse_index_convert(torch.from_numpy(req).to(dev), torch.from_numpy(bt).to(dev),
+                               torch.from_numpy(ti).to(dev), block_size=bs, out=out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().astype(np.int64), want)
+
+
+def test_index_convert_ragged_bit_exact():
+    T, topk = 9, 256
+    req, bt, ti = _convert_case(3, T, topk, 5, 20, 64)
+    rng = np.random.default_rng(4)
+    lens = rng.integers(0, topk + 1, size=T)
+    lens[0], lens[1] = 0, topk
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    init = np.full(T * topk, 99, dtype=np.int64)
+    want = O.index_convert(req, bt, ti, 64, cu_seqlens=cu, out_init=init)
+    dev = torch.device("cuda")
+    out = torch.full((T * topk,), 99, dtype=torch.int32, device=dev)
+    B.mla_sparse_index_convert(torch.from_numpy(req).to(dev), torch.from_numpy(bt).to(dev),
+                               torch.from_numpy(ti).to(dev), block_size=64,
+                               cu_seqlens=torch.from_numpy(cu).to(dev), out=out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().astype(np.int64), want)
+
+
+def test_index_convert_strided_inputs():
+    T, topk = 6, 128
+    req, bt, ti = _convert_case(5, T, topk, 4, 10, 16)
+    want = O.index_convert(req, bt, ti, 16)
+    dev = torch.device("cuda")
+    bt_wide = torch.zeros((4, 17), dtype=torch.int32, device=dev)
+    bt_wide[:, :10] = torch.from_numpy(bt).to(dev)
+    ti_wide = torch.zeros((T, 200), dtype=torch.int32, device=dev)
+    ti_wide[:, :topk] = torch.from_numpy(ti).to(dev)
+    out = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    B.mla_sparse_index_convert(torch.from_numpy(req).to(dev), bt_wide[:, :10], ti_wide[:, :topk],
+                               block_size=16, out=out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().astype(np.int64), want)
+
+
+# ---------------------------------------------------------------- merge kernel
+
+@pytest.mark.parametrize("sinks", [False, True])
+@pytest.mark.parametrize("ns,tile", [(1, 16), (4, 16), (5, 64), (16, 1)])
+def test_merge_kernel_matches_oracle(ns, tile, sinks):
+    rng = np.random.default_rng(ns * 10 + tile + sinks)
+    T, H = 7, 12
+    lens = np.array([0, 1, 17, 64, 65, 300, 5000], dtype=np.int32)
+    so = rng.standard_normal((T, H, ns, 512)).astype(np.float32)
+    sm = (rng.standard_normal((T, H, ns)) * 6).astype(np.float32)
+    se = rng.uniform(0.5, 40, (T, H, ns)).astype(np.float32)
+    for t in range(T):
+        for s, (a, b) in enumerate(O.segment_bounds(int(lens[t]), ns, tile)):
+            if a >= lens[t]:                  # dead segment: garbage the merge must skip
+                so[t, :, s] = np.nan
+                sm[t, :, s] = np.nan
+                se[t, :, s] = np.nan
+    se[5, 3, 0] = 0.0                          # a fully masked live segment
+    sm[5, 3, 0] = -np.inf
+    so[5, 3, 0] = 0.0
+    sk = rng.standard_normal(H).astype(np.float32) if sinks else None
+    ref_o, ref_l = O.merge_segments(so.astype(np.float64), sm, se, lens, tile, sinks=sk)
+    dev = torch.device("cuda")
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    B.mla_merge_segments(torch.from_numpy(so).to(dev), torch.from_numpy(sm).to(dev),
+                         torch.from_numpy(se).to(dev), torch.from_numpy(lens).to(dev),
+                         tile_size=tile, sinks=None if sk is None else torch.from_numpy(sk).to(dev),
+                         out=out, lse=lse)
+    torch.cuda.synchronize()
+    o = out.float().cpu().numpy()
+    l = lse.cpu().numpy()
+    # the merge itself only rounds: fp32 accumulation and the bf16 output
+    assert np.isfinite(o).all()
+    assert np.max(np.abs(o - ref_o) / (np.abs(ref_o) + 1e-3)) < 1e-2
+    assert_close(o, l, ref_o, ref_l, "bf16", "merge")
+
+
+# ---------------------------------------------------------------- dense decode
+
+def test_tiny_dense_full_parity():
+    w = I.tiny_dense()
+    out, lse, dw = run_gpu(w)
+    assert dw.plan.num_segments == 4 and dw.plan.tile_size == 16
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", "tiny dense")
+
+
+def test_tiny_dense_segment_partials():
+    w = I.tiny_dense()
+    dw = B.DeviceWorkload(w)
+    T, H, NS = w.num_tokens, w.num_heads, dw.plan.num_segments
+    dev = dw.device
+    so = torch.empty((T, H, NS, 512), dtype=torch.float32, device=dev)
+    sm = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
+    se = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
+    B.mla_decode_segments(dw.plan, dw.q, dw.cache, block_table=dw.block_table,
+                          seq_lens=dw.seq_lens, softmax_scale=w.softmax_scale,
+                          segm_output=so, segm_max=sm, segm_expsum=se)
+    torch.cuda.synchronize()
+    ro, rm, re = O.segment_partials(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, w.block_table,
+                                    w.seq_lens, w.softmax_scale, NS, dw.plan.tile_size)
+    so, sm, se = so.cpu().numpy(), sm.cpu().numpy(), se.cpu().numpy()
+    assert np.array_equal(np.isneginf(sm), np.isneginf(rm))
+    assert np.array_equal(se == 0, re == 0)
+    live = re > 0
+    assert np.max(np.abs(sm[live] - rm[live])) < 1e-3
+    assert np.max(np.abs(se[live] / re[live] - 1)) < 5e-3
+    assert np.max(np.abs(so - ro)) < 1e-2
+    # merging the GPU partials with the oracle merge gives the unsplit result
+    mo, ml = O.merge_segments(so, sm, se, O.partition_lengths(w.seq_lens), dw.plan.tile_size)
+    uo, ul = run_oracle(w)
+    assert_close(mo, ml, uo, ul, "bf16", "oracle merge of gpu partials")
+
+
+@pytest.mark.parametrize("ns", [0, 1, 2, 3, 7])
+def test_dsv3_shaped_bf16(ns):
+    w = I.dsv3_bf16(batch=6, seq_lo=1024, seq_hi=2100, num_segments=ns)
+    out, lse, dw = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", f"dsv3 ns={dw.plan.num_segments}")
+
+
+@pytest.mark.parametrize("heads", [16, 32, 48, 64, 96, 128])
+def test_fp8_heads(heads):
+    w = I.fp8_decode(heads, batch=3, seq_len=2048)
+    out, lse, _ = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "fp8", f"fp8 H={heads}")
+
+
+@pytest.mark.parametrize("ns", [0, 1, 4])
+def test_multi_token_with_sinks(ns):
+    w = I.mtp_sinks(batch=6, median=700, lo=128, hi=2048, num_segments=ns)
+    out, lse, _ = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", "mtp+sinks")
+
+
+@pytest.mark.parametrize("heads,bs,ns,sinks", [
+    (1, 16, 1, False), (5, 16, 4, True), (16, 16, 3, False), (20, 8, 2, True),
+    (48, 16, 1, True), (128, 16, 5, False)])
+def test_edge_lengths(heads, bs, ns, sinks):
+    seq = [0, 1, 15, 16, 17, 63, 64, 65, 200]
+    w = I.build_dense(77 + heads, seq_lens=seq, num_heads=heads, block_size=bs,
+                      with_sinks=sinks, num_segments=ns)
+    out, lse, _ = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", "edge lengths")
+    if not sinks:
+        assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
+
+
+@pytest.mark.parametrize("bs", [1, 8, 48, 128, 256])
+def test_block_sizes(bs):
+    w = I.build_dense(90 + bs, seq_lens=[3, 300, 513], num_heads=16, block_size=bs,
+                      num_segments=0)
+    out, lse, dw = run_gpu(w)
+    assert dw.plan.tile_size == O.tile_size_for_block(bs)
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", f"block {bs}")
+
+
+def test_multi_token_rows_and_short_sequences():
+    # qlen larger than 1 with a sequence shorter than the block: the first
+    # rows see very few keys.
+    w = I.build_dense(5, seq_lens=[4, 2, 9], num_heads=128, block_size=64, qlens=[4, 2, 3],
+                      with_sinks=False, num_segments=2)
+    out, lse, _ = run_gpu(w)
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", "short mtp")
+
+
+# ---------------------------------------------------------------- sparse decode
+
+@pytest.mark.parametrize("ns", [0, 1, 4])
+def test_sparse_small(ns):
+    w = I.sparse_topk(num_reqs=3, tokens_per_req=4, cache_tokens=4096, topk=512,
+                      interspersed_rows=2, max_pad=64, num_segments=ns)
+    out, lse, dw = run_gpu(w)
+    assert np.array_equal(dw.slots.cpu().numpy().astype(np.int64), oracle_slots(w))
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", "sparse")
+
+
+def test_sparse_ragged_indptr():
+    w = I.sparse_topk(num_reqs=2, tokens_per_req=3, cache_tokens=2048, topk=256, max_pad=0)
+    slots = oracle_slots(w)
+    lens = np.array([256, 0, 17, 128, 255, 1])
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    flat = np.concatenate([slots[t, :lens[t]] for t in range(6)]).astype(np.int32)
+    dw = B.DeviceWorkload(w, num_segments=3)
+    dev = dw.device
+    B.mla_decode_fwd(dw.plan, dw.q, dw.cache, sparse_slots=torch.from_numpy(flat).to(dev),
+                     sparse_indptr=torch.from_numpy(cu).to(dev), softmax_scale=w.softmax_scale,
+                     workspace=dw.workspace, out=dw.out, lse=dw.lse)
+    torch.cuda.synchronize()
+    ref_o, ref_l = O.mla_decode(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, None, None,
+                                w.softmax_scale, sparse_slots=flat, sparse_indptr=cu)
+    assert_close(dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), ref_o, ref_l, "bf16",
+                 "sparse ragged")
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_rerun_and_page_permutation_are_bit_identical():
+    w = I.dsv3_bf16(batch=5, seq_lo=300, seq_hi=1500, num_segments=3)
+    out1, lse1, _ = run_gpu(w)
+    out2, lse2, _ = run_gpu(w)
+    assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
+    rng = np.random.default_rng(9)
+    perm = rng.permutation(w.num_blocks)
+    cache2 = np.empty_like(w.cache)
+    cache2[perm] = w.cache
+    w.cache = cache2
+    w.block_table = perm[w.block_table].astype(np.int32)
+    out3, lse3, _ = run_gpu(w)
+    assert np.array_equal(out1, out3) and np.array_equal(lse1, lse3)
+
+
+def test_side_stream_and_graph_replay():
+    w = I.dsv3_bf16(batch=4, seq_lo=200, seq_hi=900, num_segments=2)
+    ref_o, ref_l = run_oracle(w)
+    dw = B.DeviceWorkload(w)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dw.forward()
+        dw.forward()
+    torch.cuda.synchronize()
+    assert_close(dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), ref_o, ref_l, "bf16",
+                 "side stream")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dw.forward()
+    # replay with shorter sequences written into the same device buffer
+    w2 = I.dsv3_bf16(batch=4, seq_lo=200, seq_hi=900, num_segments=2)
+    w2.seq_lens = np.maximum(w.seq_lens - 37, 1).astype(np.int32)
+    dw.seq_lens.copy_(torch.from_numpy(w2.seq_lens))
+    dw.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    ro2, rl2 = run_oracle(w2)
+    assert_close(dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), ro2, rl2, "bf16",
+                 "graph replay")
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def _sampled(w, tokens, ns=None):
+    out, lse, dw = run_gpu(w, num_segments=ns)
+    ref_o, ref_l = run_oracle(w, tokens=tokens)
+    return out[tokens], lse[tokens], ref_o, ref_l, dw
+
+
+def test_full_dsv3_bf16_sampled():
+    w = I.dsv3_bf16()
+    order = np.argsort(w.seq_lens)
+    tokens = sorted({int(order[0]), int(order[-1]), 5, 31, 63})
+    out, lse, ro, rl, dw = _sampled(w, tokens)
+    assert_close(out, lse, ro, rl, "bf16", f"full dsv3 ns={dw.plan.num_segments}")
+
+
+@pytest.mark.parametrize("heads", [16, 128])
+def test_full_fp8_sampled(heads):
+    w = I.fp8_decode(heads)
+    out, lse, ro, rl, _ = _sampled(w, [0, 25, 51])
+    assert_close(out, lse, ro, rl, "fp8", f"full fp8 H={heads}")
+
+
+def test_full_mtp_sinks_sampled():
+    w = I.mtp_sinks()
+    T = w.num_tokens
+    out, lse, ro, rl, _ = _sampled(w, [0, 1, T // 2, T - 1])
+    assert_close(out, lse, ro, rl, "bf16", "full mtp+sinks")
+
+
+def test_full_sparse_sampled():
+    w = I.sparse_topk(interspersed_rows=1)
+    out, lse, dw = run_gpu(w)
+    slots = oracle_slots(w)
+    assert np.array_equal(dw.slots.cpu().numpy().astype(np.int64), slots)
+    tokens = [0, 1, 64, 127]
+    ro, rl = run_oracle(w, tokens=tokens, slots=slots)
+    assert_close(out[tokens], lse[tokens], ro, rl, "bf16", "full sparse")
