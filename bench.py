@@ -1,0 +1,444 @@
+"""Benchmark of the paged MLA decode hot path on one or more GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+A step is one full decode call (split-K segments + merge, through the C ABI)
+over one batch of the DeepSeek-V3-shaped bf16 workload: 64 requests, 128
+heads, qlen 1, seq_lens uniform in [1024, 8192], block 64, values ~N(0, 1),
+random page permutation, segments chosen by the planner. Inputs are seeded
+and synthetic. L2 is flushed (a 256 MiB write) before every timed step, and
+only the step itself is inside its CUDA events.
+
+Under torchrun (N > 1) every rank decodes its own batch of the same shape
+(weak scaling, no collective on the data path); the per-step time is the max
+over ranks and ``value`` counts the KV tokens of all ranks.
+
+``--impl reference`` times the fp64 CPU oracle on the host cores instead (a
+bounded sample of the same workload) and prints the same JSON line with
+``"impl": "reference"``.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("MLA decode µs/call & KV tokens/s; HBM GB/s or MMA util as % of GB300 "
+          "roofline")
+UNIT = "KV tokens/s"
+WORKLOAD = ("dsv3_bf16: DeepSeek-V3-shaped bf16 MLA decode, batch 64, 128 heads, qlen 1, "
+            "seq_lens uniform in [1024, 8192], block_size 64, q/cache ~N(0,1) bf16, "
+            "scale 1/sqrt(192), random page permutation, segments chosen by the planner")
+KV_ROW_BYTES = 576 * 2          # one bf16 cache row
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def _workload(seed_offset=0):
+    from paged_mla_decode_06_gb300 import inputs as I
+    return I.dsv3_bf16(seed=2 + seed_offset)
+
+
+def _flops(w):
+    # 2176 flop per (key, row): 1152 for q.k over 576 columns, 1024 for p.v over 512
+    return float(w.seq_lens.astype("int64").sum()) * w.num_heads * 2176.0
+
+
+def _alg_bytes_decode(w):
+    """Algorithmic bytes of one decode launch: every KV row once, q once, the
+    block-table entries read. Segment partials are not algorithmic."""
+    import numpy as np
+    keys = int(w.seq_lens.astype(np.int64).sum())
+    blocks = int(((w.seq_lens.astype(np.int64) + w.block_size - 1) // w.block_size).sum())
+    return keys * KV_ROW_BYTES + w.num_tokens * w.num_heads * 576 * 2 + blocks * 4 + \
+        w.num_reqs * 4
+
+
+def _alg_bytes_step(w):
+    return _alg_bytes_decode(w) + w.num_tokens * w.num_heads * (512 * 2 + 4)
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, log_path: str | None = None):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.log_path = log_path
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        if self.log_path:
+            with open(self.log_path, "w") as f:
+                f.write(self.FIELDS + "\n" + "\n".join(self.lines) + "\n")
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s >= 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline: the oracle as it stands, on the host cores
+# ---------------------------------------------------------------------------
+
+def _oracle_worker(budget_s, n_steps, q):
+    """Time the oracle on bounded samples of the workload: each step runs
+    requests (continuing round-robin through the batch) until ``budget_s``
+    seconds have passed, at least one request per step."""
+    import numpy as np
+    import oracle as O
+    from paged_mla_decode_06_gb300 import inputs as I
+
+    w = I.dsv3_bf16()
+    blas = "unknown"
+    try:
+        cfg = np.show_config(mode="dicts")
+        blas = cfg.get("Build Dependencies", {}).get("blas", {}).get("name", "unknown")
+    except Exception:  # noqa: BLE001
+        pass
+    r = 0
+    out = []
+    for _ in range(n_steps):
+        keys = 0
+        done = 0
+        t0 = time.perf_counter()
+        while True:
+            O.mla_decode(w.q[r:r + 1], "bf16", 1.0, w.cache, "bf16", 1.0,
+                         w.block_table[r:r + 1], w.seq_lens[r:r + 1], w.softmax_scale,
+                         block_size=w.block_size)
+            keys += int(w.seq_lens[r])
+            done += 1
+            r = (r + 1) % w.num_reqs
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        out.append({"keys": keys, "requests": done, "seconds": time.perf_counter() - t0})
+    q.put({"steps": out, "blas": blas, "total_requests": w.num_reqs})
+
+
+def cpu_baseline_steps(budget_s=20.0, n_steps=1):
+    """Run the oracle in a fresh (spawned) process whose BLAS uses every host
+    core; returns one record per step."""
+    cores = os.cpu_count() or 1
+    env_keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = str(cores)
+    try:
+        ctx = mp.get_context("spawn")
+        q = ctx.Queue()
+        p = ctx.Process(target=_oracle_worker, args=(budget_s, n_steps, q))
+        p.start()
+        res = q.get(timeout=1800)
+        p.join(timeout=60)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    recs = []
+    for st in res["steps"]:
+        recs.append({"value": st["keys"] / st["seconds"], "unit": UNIT, "cores": cores,
+                     "kind": "oracle",
+                     "sample": (f"fp64 numpy oracle, {st['requests']} request decodes taken "
+                                f"round-robin from the {res['total_requests']}-request batch "
+                                f"({st['keys']} KV tokens, {st['seconds']:.1f} s, "
+                                f"BLAS {res['blas']} with {cores} threads)"),
+                     "seconds": st["seconds"]})
+    return recs
+
+
+def cpu_baseline(budget_s=20.0):
+    return cpu_baseline_steps(budget_s, 1)[0]
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from paged_mla_decode_06_gb300 import binding as B
+    from paged_mla_decode_06_gb300 import build as BUILD
+
+    BUILD.build()
+    B.load_library()
+    w = _workload(seed_offset=rank)
+    dw = B.DeviceWorkload(w, device=dev)
+    plan = dw.plan
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    # ---- device-resident timing of the whole step
+    for _ in range(args.warmup):
+        dw.forward()
+    barrier()
+    sampler = ClockSampler(dev.index or 0, os.path.join(ROOT, "gpurun_out", "clocks.csv")
+                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    sampler.start()
+    barrier()
+    t_wall = time.perf_counter()
+    step_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dw.forward()
+        e1.record(stream)
+        e1.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+    barrier()
+    wall = time.perf_counter() - t_wall
+
+    # ---- the decode kernel alone (same launch as inside the step)
+    T, H, NS = w.num_tokens, w.num_heads, plan.num_segments
+    so = torch.empty((T, H, NS, 512), dtype=torch.float32, device=dev)
+    sm = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
+    se = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
+
+    def decode_only():
+        B.mla_decode_segments(plan, dw.q, dw.cache, block_table=dw.block_table,
+                              seq_lens=dw.seq_lens, softmax_scale=w.softmax_scale,
+                              segm_output=so, segm_max=sm, segm_expsum=se)
+
+    for _ in range(3):
+        decode_only()
+    dec_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        decode_only()
+        e1.record(stream)
+        e1.synchronize()
+        dec_ms.append(e0.elapsed_time(e1))
+    clocks = sampler.stop()
+
+    # ---- end to end through the C ABI with host buffers
+    h_q = torch.from_numpy(w.q.view(np.int16)).pin_memory()
+    h_bt = torch.from_numpy(w.block_table).pin_memory()
+    h_sl = torch.from_numpy(w.seq_lens).pin_memory()
+    h_out = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    h2d = h_q.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def e2e_step():
+        dw.q.copy_(h_q, non_blocking=True)
+        dw.block_table.copy_(h_bt, non_blocking=True)
+        dw.seq_lens.copy_(h_sl, non_blocking=True)
+        dw.forward()
+        h_out.copy_(dw.out, non_blocking=True)
+        h_lse.copy_(dw.lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+
+    keys_rank = float(w.seq_lens.astype(np.int64).sum())
+    ms = statistics.mean(step_ms)
+    dms = statistics.mean(dec_ms)
+    ems = statistics.mean(e2e_ms)
+    if world > 1:
+        t = torch.tensor([ms, dms, ems, keys_rank], dtype=torch.float64, device=dev)
+        mx = t.clone()
+        dist.all_reduce(mx[:3], op=dist.ReduceOp.MAX)
+        ks = t[3:].clone()
+        dist.all_reduce(ks, op=dist.ReduceOp.SUM)
+        ms, dms, ems = (float(x) for x in mx[:3].tolist())
+        keys_total = float(ks.item())
+    else:
+        keys_total = keys_rank
+
+    if rank == 0:
+        peaks, src = _peaks()
+        alg = _alg_bytes_decode(w)
+        achieved = alg / (dms * 1e-3) / 1e9
+        peak_bw = float(peaks["hbm_gbs"])
+        tflops = _flops(w) / (dms * 1e-3) / 1e12
+        line = {
+            "metric": METRIC,
+            "value": keys_total / (ms * 1e-3),
+            "unit": UNIT,
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms,
+            "us_per_call": ms * 1e3,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "bf16",
+            "data": "synthetic (seeded numpy; no dataset or weights)",
+            "config": {"workload": WORKLOAD, "num_segments": NS, "tile_size": plan.tile_size,
+                       "rows_per_cta": plan.rows_per_cta, "kernel": int(plan.kernel),
+                       "kv_tokens_per_gpu": int(keys_rank),
+                       "l2": "flushed (256 MiB write) before every timed step",
+                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
+                         "frac": achieved / peak_bw, "traffic": None,
+                         "kernel": "decode_mma_kernel (split-K segments)",
+                         "kernel_us": dms * 1e3, "algorithmic_bytes": alg,
+                         "peak_source": f"hbm_gbs of {src}",
+                         "tensor_tflops": tflops,
+                         "tensor_frac": tflops / float(peaks.get("bf16_tflops", 1900.0))},
+            "clocks": clocks,
+            "e2e": {"value": keys_total / (ems * 1e-3), "unit": UNIT,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": ems},
+            "gpu_launches": args.steps * (1 + (1 if NS > 1 else 0)),
+            "wall_s_timed_region": wall,
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+        else:
+            line["cpu_baseline"] = None
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    n = args.warmup + args.steps
+    budget = min(10.0, max(1.0, 90.0 / n))
+    recs = cpu_baseline_steps(budget, n)[args.warmup:]
+    value = statistics.mean(r["value"] for r in recs)
+    ms = statistics.mean(1e3 * r["seconds"] for r in recs)
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded numpy; no dataset or weights)",
+        "config": {"workload": WORKLOAD,
+                   "sample": f"each step a bounded sample (~{budget:.1f} s) of the batch"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": recs[0]["cores"],
+                         "kind": "oracle", "sample": recs[-1]["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

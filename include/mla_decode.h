@@ -94,7 +94,18 @@ typedef struct {
   int32_t has_sinks;           /* 1 when a sinks array will be passed */
   int32_t num_segments;        /* split-K segments per row; 0 lets the planner choose */
   int32_t num_sms;             /* SMs to plan for; 0 queries the current device */
+  int32_t kernel;              /* 0 lets the planner choose the decode kernel; else a
+                                  mla_kernel_t value (MLA_ERR_UNSUPPORTED if it cannot
+                                  run this problem) */
 } mla_problem_t;
+
+/* Decode kernel variants. */
+typedef enum {
+  MLA_KERNEL_AUTO = 0,
+  MLA_KERNEL_WARP_MMA = 1,     /* warp-level MMA split-K kernel: every shape */
+  MLA_KERNEL_TCGEN05 = 2       /* tcgen05/TMEM CTA-pair kernel: dense bf16,
+                                  block_size a multiple of 64 */
+} mla_kernel_t;
 
 /* Filled by mla_decode_plan; pass it unchanged to mla_decode_fwd or
  * mla_decode_segments. */
@@ -109,9 +120,11 @@ typedef struct {
   int32_t grid_x, grid_y, grid_z;
   int32_t num_sms;
   int32_t reserved[4];
-  size_t workspace_bytes;      /* bytes mla_decode_fwd needs; 0 when NS == 1 */
-  size_t segm_max_offset;      /* workspace layout: segm_output at offset 0, */
-  size_t segm_expsum_offset;   /* then segm_max, then segm_expsum (256-B aligned) */
+  size_t workspace_bytes;      /* bytes mla_decode_fwd needs (>= 256) */
+  size_t status_offset;        /* workspace layout, 256-B aligned pieces: a device */
+  size_t segm_output_offset;   /* status word (int32) at offset 0, then, when */
+  size_t segm_max_offset;      /* NS > 1, segm_output, segm_max and segm_expsum */
+  size_t segm_expsum_offset;
 } mla_plan_t;
 
 /*
@@ -152,8 +165,12 @@ MLA_API mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan
  *   sinks        [H] fp32 natural-log sink logits or NULL ([sparse]
  *                _forward_mla): a sink adds e^sink to the softmax denominator
  *                and nothing to the output.
- *   workspace    plan->workspace_bytes of device memory (NULL allowed when
- *                that is 0); contents need not be initialised.
+ *   workspace    plan->workspace_bytes of device memory, 256-byte aligned.
+ *                Its first int32 is a device status word that must be zero
+ *                before the first call (zero it once after allocating): the
+ *                tensor-core kernel writes a nonzero code there, and leaves
+ *                its outputs unwritten, if one of its bounded internal waits
+ *                times out. The rest needs no initialisation.
  *   out          [T, H, 512] bf16; lse [T, H] fp32 natural log. Every element
  *                is written; a row with no visible key gets out = 0 and
  *                lse = -inf (or its sink).

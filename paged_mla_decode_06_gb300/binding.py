@@ -22,6 +22,10 @@ MLA_ERR_CUDA = 4
 MLA_DTYPE_BF16 = 0
 MLA_DTYPE_FP8_E4M3 = 1
 
+MLA_KERNEL_AUTO = 0
+MLA_KERNEL_WARP_MMA = 1
+MLA_KERNEL_TCGEN05 = 2
+
 HEAD_DIM = 576
 KV_LORA_RANK = 512
 
@@ -40,7 +44,7 @@ class Problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_tokens", "num_reqs", "num_heads", "head_dim", "kv_lora_rank", "block_size",
         "max_blocks_per_req", "num_blocks", "max_seq_len", "max_qlen", "topk", "q_dtype",
-        "kv_dtype", "has_sinks", "num_segments", "num_sms")]
+        "kv_dtype", "has_sinks", "num_segments", "num_sms", "kernel")]
 
 
 class Plan(ctypes.Structure):
@@ -48,6 +52,8 @@ class Plan(ctypes.Structure):
         "num_segments", "tile_size", "kernel", "rows_per_cta", "row_tiles", "grid_x", "grid_y",
         "grid_z", "num_sms")] + [("reserved", ctypes.c_int32 * 4),
                                  ("workspace_bytes", ctypes.c_size_t),
+                                 ("status_offset", ctypes.c_size_t),
+                                 ("segm_output_offset", ctypes.c_size_t),
                                  ("segm_max_offset", ctypes.c_size_t),
                                  ("segm_expsum_offset", ctypes.c_size_t)]
 
@@ -139,13 +145,15 @@ def _dtype_code(name: str) -> int:
 def make_problem(*, num_tokens: int, num_heads: int, block_size: int, num_blocks: int,
                  num_reqs: int = 0, max_blocks_per_req: int = 0, max_seq_len: int = 0,
                  max_qlen: int = 1, topk: int = 0, dtype: str = "bf16",
-                 has_sinks: bool = False, num_segments: int = 0, num_sms: int = 0) -> Problem:
+                 has_sinks: bool = False, num_segments: int = 0, num_sms: int = 0,
+                 kernel: int = MLA_KERNEL_AUTO) -> Problem:
     return Problem(num_tokens=num_tokens, num_reqs=num_reqs, num_heads=num_heads,
                    head_dim=HEAD_DIM, kv_lora_rank=KV_LORA_RANK, block_size=block_size,
                    max_blocks_per_req=max_blocks_per_req, num_blocks=num_blocks,
                    max_seq_len=max_seq_len, max_qlen=max_qlen, topk=topk,
                    q_dtype=_dtype_code(dtype), kv_dtype=_dtype_code(dtype),
-                   has_sinks=int(bool(has_sinks)), num_segments=num_segments, num_sms=num_sms)
+                   has_sinks=int(bool(has_sinks)), num_segments=num_segments, num_sms=num_sms,
+                   kernel=kernel)
 
 
 def mla_decode_plan(problem: Problem) -> Plan:
@@ -213,7 +221,8 @@ def mla_sparse_index_convert(req_id, block_table, token_indices, *, block_size: 
 class DeviceWorkload:
     """Device copies of an ``inputs.Workload`` plus a plan and output buffers."""
 
-    def __init__(self, w, device="cuda", num_segments=None, num_sms=0, plan=True):
+    def __init__(self, w, device="cuda", num_segments=None, num_sms=0, plan=True,
+                 kernel=MLA_KERNEL_AUTO):
         import torch
 
         self.w = w
@@ -240,11 +249,16 @@ class DeviceWorkload:
             max_blocks_per_req=w.max_blocks_per_req,
             max_seq_len=int(w.seq_lens.max()) if w.num_reqs else 0,
             max_qlen=w.max_qlen, topk=w.topk, dtype=w.kv_dtype, has_sinks=w.sinks is not None,
-            num_segments=ns, num_sms=num_sms)
+            num_segments=ns, num_sms=num_sms, kernel=kernel)
         self.plan = mla_decode_plan(self.problem) if plan else None
         self.workspace = None
         if self.plan is not None and self.plan.workspace_bytes:
-            self.workspace = torch.empty(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)
+            # zeroed once: its first int32 is the device status word
+            self.workspace = torch.zeros(self.plan.workspace_bytes, dtype=torch.uint8, device=dev)
+
+    def status(self) -> int:
+        """Device status word of the workspace (0 = no kernel reported a timeout)."""
+        return int(self.workspace[:4].view(torch.int32).item()) if self.workspace is not None else 0
 
     def convert(self, stream=None):
         """Top-k positions -> global slots (sparse workloads)."""

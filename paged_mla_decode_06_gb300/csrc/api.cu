@@ -47,6 +47,7 @@ mla_status_t check_problem(const mla_problem_t& p) {
   if (p.num_segments < 0 || p.num_segments > kMaxSegments) return MLA_ERR_INVALID_ARG;
   if (p.num_sms < 0 || p.has_sinks < 0 || p.has_sinks > 1) return MLA_ERR_INVALID_ARG;
   if (p.topk < 0) return MLA_ERR_INVALID_ARG;
+  if (p.kernel < MLA_KERNEL_AUTO || p.kernel > MLA_KERNEL_TCGEN05) return MLA_ERR_INVALID_ARG;
   if (p.topk > 0) {
     if (p.topk % 128 != 0) return MLA_ERR_UNSUPPORTED;
     if (p.max_qlen > 1) return MLA_ERR_INVALID_ARG;  // sparse rows are single tokens
@@ -149,6 +150,19 @@ dim3 grid_of(const mla_plan_t* plan) {
               static_cast<unsigned>(plan->grid_z));
 }
 
+mla_status_t launch_decode(const mla_plan_t* plan, const mla::DecodeParams& d, int* status,
+                           cudaStream_t stream) {
+  if (plan->grid_z == 0) return MLA_OK;
+  const mla_problem_t& p = plan->prob;
+  if (plan->kernel == mla::kTcPair128) {
+    const int64_t q_rows = static_cast<int64_t>(p.num_tokens) * p.num_heads;
+    const int64_t kv_rows = static_cast<int64_t>(p.num_blocks) * p.block_size;
+    return cuda_status(mla::launch_decode_tc(d, q_rows, kv_rows, grid_of(plan), status, stream));
+  }
+  return cuda_status(mla::launch_decode_mma(plan->kernel, p.kv_dtype == MLA_DTYPE_FP8_E4M3, d,
+                                            grid_of(plan), stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -188,8 +202,14 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   const bool sparse = p.topk > 0;
   const int32_t units = sparse ? p.num_tokens : p.num_reqs;
   const int64_t rows_per_unit = sparse ? p.num_heads : static_cast<int64_t>(p.num_heads) * p.max_qlen;
+  const bool tc_ok = !sparse && p.kv_dtype == MLA_DTYPE_BF16 && p.block_size % 64 == 0;
+  if (p.kernel == MLA_KERNEL_TCGEN05 && !tc_ok) return MLA_ERR_UNSUPPORTED;
+  const bool use_tc = tc_ok && p.kernel != MLA_KERNEL_WARP_MMA;
   int32_t kernel, rows;
-  if (rows_per_unit <= 16) {
+  if (use_tc) {
+    kernel = mla::kTcPair128;
+    rows = 128;
+  } else if (rows_per_unit <= 16) {
     kernel = mla::kMmaRows16;
     rows = 16;
   } else if (rows_per_unit <= 32) {
@@ -220,16 +240,19 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   plan->kernel = kernel;
   plan->rows_per_cta = rows;
   plan->row_tiles = row_tiles;
-  plan->grid_x = row_tiles;
+  plan->grid_x = use_tc ? 2 * row_tiles : row_tiles;  // a CTA pair per row tile
   plan->grid_y = ns;
   plan->grid_z = units;
+  plan->status_offset = 0;
+  plan->workspace_bytes = kWsAlign;
   if (ns > 1) {
     const size_t th = static_cast<size_t>(p.num_tokens) * p.num_heads;
     const size_t out_b = align_up(th * ns * kRank * sizeof(float), kWsAlign);
     const size_t max_b = align_up(th * ns * sizeof(float), kWsAlign);
-    plan->segm_max_offset = out_b;
-    plan->segm_expsum_offset = out_b + max_b;
-    plan->workspace_bytes = out_b + 2 * max_b;
+    plan->segm_output_offset = kWsAlign;
+    plan->segm_max_offset = kWsAlign + out_b;
+    plan->segm_expsum_offset = kWsAlign + out_b + max_b;
+    plan->workspace_bytes = kWsAlign + out_b + 2 * max_b;
   }
   return MLA_OK;
 }
@@ -255,9 +278,7 @@ mla_status_t mla_decode_segments(const mla_plan_t* plan, const void* q, const vo
   d.segm_out = segm_output;
   d.segm_max = segm_max;
   d.segm_expsum = segm_expsum;
-  if (plan->grid_z == 0) return MLA_OK;
-  return cuda_status(mla::launch_decode_mma(plan->kernel, plan->prob.kv_dtype == MLA_DTYPE_FP8_E4M3,
-                                            d, grid_of(plan), stream));
+  return launch_decode(plan, d, nullptr, stream);
 }
 
 mla_status_t mla_decode_fwd(const mla_plan_t* plan, const void* q, const void* kv_cache,
@@ -277,29 +298,24 @@ mla_status_t mla_decode_fwd(const mla_plan_t* plan, const void* q, const void* k
   if (out == nullptr || lse == nullptr || !aligned(out, 16) || !aligned(lse, 4))
     return MLA_ERR_INVALID_ARG;
   if (sinks != nullptr && !aligned(sinks, 4)) return MLA_ERR_INVALID_ARG;
-  if (plan->workspace_bytes > 0) {
-    if (workspace == nullptr || workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE;
-    if (!aligned(workspace, kWsAlign)) return MLA_ERR_INVALID_ARG;
-  }
+  if (workspace == nullptr || workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE;
+  if (!aligned(workspace, kWsAlign)) return MLA_ERR_INVALID_ARG;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* status = reinterpret_cast<int*>(ws + plan->status_offset);
   mla::DecodeParams d = make_params(plan, in);
-  const bool fp8 = p.kv_dtype == MLA_DTYPE_FP8_E4M3;
   if (plan->num_segments == 1) {
     d.final_mode = 1;
     d.sinks = sinks;
     d.out = out;
     d.lse = lse;
-    if (plan->grid_z == 0) return MLA_OK;
-    return cuda_status(mla::launch_decode_mma(plan->kernel, fp8, d, grid_of(plan), stream));
+    return launch_decode(plan, d, status, stream);
   }
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
   d.final_mode = 0;
-  d.segm_out = reinterpret_cast<float*>(ws);
+  d.segm_out = reinterpret_cast<float*>(ws + plan->segm_output_offset);
   d.segm_max = reinterpret_cast<float*>(ws + plan->segm_max_offset);
   d.segm_expsum = reinterpret_cast<float*>(ws + plan->segm_expsum_offset);
-  if (plan->grid_z > 0) {
-    s = cuda_status(mla::launch_decode_mma(plan->kernel, fp8, d, grid_of(plan), stream));
-    if (s != MLA_OK) return s;
-  }
+  s = launch_decode(plan, d, status, stream);
+  if (s != MLA_OK) return s;
   mla::MergeParams m{};
   m.segm_out = d.segm_out;
   m.segm_max = d.segm_max;

@@ -12,6 +12,7 @@ enum KernelId : int32_t {
   kMmaRows16 = 1,   // warp-MMA split-K kernel, 16 query rows per CTA
   kMmaRows32 = 2,   // 32 rows per CTA
   kMmaRows64 = 3,   // 64 rows per CTA
+  kTcPair128 = 4,   // tcgen05 CTA-pair kernel, 128 rows per pair
 };
 
 struct DecodeParams {
@@ -67,7 +68,14 @@ cudaError_t launch_index_convert(const int32_t* req_id, const int32_t* block_tab
                                  int32_t num_tokens, int32_t topk, int32_t block_size,
                                  const int32_t* cu_seqlens, int32_t* out, cudaStream_t stream);
 
+// tcgen05 CTA-pair kernel: q_rows / kv_rows are the row counts of the q
+// and cache tensors viewed as [rows, 576]; status (may be null) receives a
+// nonzero code if a bounded wait times out.
+cudaError_t launch_decode_tc(const DecodeParams& p, int64_t q_rows, int64_t kv_rows, dim3 grid,
+                             int* status, cudaStream_t stream);
+
 // Shared memory bytes a decode variant needs (host query for validation).
 int decode_mma_smem_bytes(int32_t kernel, bool fp8);
+int decode_tc_smem_bytes();
 
 }  // namespace mla

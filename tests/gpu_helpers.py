@@ -10,10 +10,11 @@ TOL_OUT = {"bf16": 1e-2, "fp8": 2e-2}
 TOL_LSE = 1e-3
 
 
-def run_gpu(w, num_segments=None, stream=None):
-    dw = B.DeviceWorkload(w, num_segments=num_segments)
+def run_gpu(w, num_segments=None, stream=None, kernel=B.MLA_KERNEL_AUTO):
+    dw = B.DeviceWorkload(w, num_segments=num_segments, kernel=kernel)
     dw.forward(stream=stream)
     torch.cuda.synchronize()
+    assert dw.status() == 0, f"device status word {dw.status()}"
     return dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), dw
 
 

@@ -40,9 +40,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_struct_sizes_match_the_header(lib):
-    assert ctypes.sizeof(B.Problem) == 16 * 4
-    # 16 problem ints + 9 plan ints + 4 reserved (+ pad) + 3 size_t
-    assert ctypes.sizeof(B.Plan) == 144
+    assert ctypes.sizeof(B.Problem) == 17 * 4
+    # 17 problem ints + 9 plan ints + 4 reserved + 5 size_t
+    assert ctypes.sizeof(B.Plan) == 160
 
 
 def test_status_strings(lib):
@@ -62,8 +62,9 @@ def _dense_problem(**kw):
 def test_plan_dense_defaults(lib):
     plan = B.mla_decode_plan(_dense_problem())
     assert plan.tile_size == 64
-    assert plan.rows_per_cta == 64 and plan.row_tiles == 2
+    assert plan.kernel == 4 and plan.rows_per_cta == 128 and plan.row_tiles == 1
     assert plan.grid_x == 2 and plan.grid_z == 64 and plan.grid_y == plan.num_segments
+    assert plan.workspace_bytes >= 256 and plan.status_offset == 0
     assert 1 <= plan.num_segments <= 16
     if plan.num_segments > 1:
         th = 64 * 128
@@ -92,6 +93,9 @@ def test_plan_explicit_segments_and_small_heads(lib):
 def test_plan_multi_token_rows(lib):
     plan = B.mla_decode_plan(_dense_problem(num_tokens=96, num_reqs=32, max_qlen=4,
                                             max_seq_len=8192))
+    assert plan.row_tiles == 4 and plan.grid_x == 8  # 4 tokens x 128 heads / 128-row pairs
+    plan = B.mla_decode_plan(_dense_problem(num_tokens=96, num_reqs=32, max_qlen=4,
+                                            max_seq_len=8192, kernel=B.MLA_KERNEL_WARP_MMA))
     assert plan.row_tiles == 8  # 4 tokens x 128 heads / 64 rows
 
 
@@ -111,6 +115,8 @@ def test_plan_sparse(lib):
     (dict(max_seq_len=100000), B.MLA_ERR_INVALID_ARG),
     (dict(max_qlen=0), B.MLA_ERR_INVALID_ARG),
     (dict(mixed_dtype=True), B.MLA_ERR_UNSUPPORTED),
+    (dict(kernel=2, block_size=16, max_blocks_per_req=600), B.MLA_ERR_UNSUPPORTED),
+    (dict(kernel=3), B.MLA_ERR_INVALID_ARG),
 ])
 def test_plan_rejects(lib, kw, status):
     kw = dict(kw)
@@ -161,6 +167,9 @@ def test_fwd_rejects_small_workspace(lib):
     plan = B.mla_decode_plan(_dense_problem(num_segments=4))
     assert plan.workspace_bytes > 0
     assert _fwd(lib, plan, wsb=plan.workspace_bytes - 1) == B.MLA_ERR_WORKSPACE
+    plan1 = B.mla_decode_plan(_dense_problem(num_segments=1))
+    assert plan1.workspace_bytes == 256
+    assert _fwd(lib, plan1, ws=None) == B.MLA_ERR_WORKSPACE
     assert _fwd(lib, plan, ws=None) == B.MLA_ERR_WORKSPACE
     assert _fwd(lib, plan, ws=FAKE + 128) == B.MLA_ERR_INVALID_ARG
 

@@ -164,12 +164,52 @@ def test_tiny_dense_segment_partials():
     assert_close(mo, ml, uo, ul, "bf16", "oracle merge of gpu partials")
 
 
+KERNELS = [B.MLA_KERNEL_WARP_MMA, B.MLA_KERNEL_TCGEN05]
+KIDS = ["mma", "tcgen05"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("ns", [0, 1, 2, 3, 7])
-def test_dsv3_shaped_bf16(ns):
+def test_dsv3_shaped_bf16(ns, kernel):
     w = I.dsv3_bf16(batch=6, seq_lo=1024, seq_hi=2100, num_segments=ns)
-    out, lse, dw = run_gpu(w)
+    out, lse, dw = run_gpu(w, kernel=kernel)
     ref_o, ref_l = run_oracle(w)
-    assert_close(out, lse, ref_o, ref_l, "bf16", f"dsv3 ns={dw.plan.num_segments}")
+    assert_close(out, lse, ref_o, ref_l, "bf16", f"dsv3 ns={dw.plan.num_segments} k={kernel}")
+
+
+@pytest.mark.parametrize("heads", [1, 16, 64, 100, 128])
+def test_tcgen05_head_counts_and_short_rows(heads):
+    # lengths around the 64-key chunk, an empty row, and a segment split
+    w = I.build_dense(60 + heads, seq_lens=[0, 1, 63, 64, 65, 127, 128, 129, 700],
+                      num_heads=heads, block_size=64, num_segments=3)
+    out, lse, dw = run_gpu(w, kernel=B.MLA_KERNEL_TCGEN05)
+    assert dw.plan.kernel == 4
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", f"tcgen05 H={heads}")
+
+
+def test_tcgen05_segment_partials():
+    w = I.build_dense(61, seq_lens=[1, 70, 300, 1000], num_heads=128, block_size=64,
+                      num_segments=4)
+    dw = B.DeviceWorkload(w, kernel=B.MLA_KERNEL_TCGEN05)
+    T, H, NS = w.num_tokens, w.num_heads, dw.plan.num_segments
+    dev = dw.device
+    so = torch.full((T, H, NS, 512), 7.0, dtype=torch.float32, device=dev)
+    sm = torch.full((T, H, NS), 7.0, dtype=torch.float32, device=dev)
+    se = torch.full((T, H, NS), 7.0, dtype=torch.float32, device=dev)
+    B.mla_decode_segments(dw.plan, dw.q, dw.cache, block_table=dw.block_table,
+                          seq_lens=dw.seq_lens, softmax_scale=w.softmax_scale,
+                          segm_output=so, segm_max=sm, segm_expsum=se)
+    torch.cuda.synchronize()
+    ro, rm, re = O.segment_partials(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, w.block_table,
+                                    w.seq_lens, w.softmax_scale, NS, dw.plan.tile_size)
+    so, sm, se = so.cpu().numpy(), sm.cpu().numpy(), se.cpu().numpy()
+    assert np.array_equal(np.isneginf(sm), np.isneginf(rm))
+    live = re > 0
+    assert np.array_equal(se > 0, live)
+    assert np.max(np.abs(sm[live] - rm[live])) < 1e-3
+    assert np.max(np.abs(se[live] / re[live] - 1)) < 5e-3
+    assert np.max(np.abs(so - ro)) < 1e-2
 
 
 @pytest.mark.parametrize("heads", [16, 32, 48, 64, 96, 128])
@@ -180,10 +220,11 @@ def test_fp8_heads(heads):
     assert_close(out, lse, ref_o, ref_l, "fp8", f"fp8 H={heads}")
 
 
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("ns", [0, 1, 4])
-def test_multi_token_with_sinks(ns):
+def test_multi_token_with_sinks(ns, kernel):
     w = I.mtp_sinks(batch=6, median=700, lo=128, hi=2048, num_segments=ns)
-    out, lse, _ = run_gpu(w)
+    out, lse, _ = run_gpu(w, kernel=kernel)
     ref_o, ref_l = run_oracle(w)
     assert_close(out, lse, ref_o, ref_l, "bf16", "mtp+sinks")
 
@@ -254,10 +295,11 @@ def test_sparse_ragged_indptr():
 
 # ---------------------------------------------------------------- invariants
 
-def test_rerun_and_page_permutation_are_bit_identical():
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_rerun_and_page_permutation_are_bit_identical(kernel):
     w = I.dsv3_bf16(batch=5, seq_lo=300, seq_hi=1500, num_segments=3)
-    out1, lse1, _ = run_gpu(w)
-    out2, lse2, _ = run_gpu(w)
+    out1, lse1, _ = run_gpu(w, kernel=kernel)
+    out2, lse2, _ = run_gpu(w, kernel=kernel)
     assert np.array_equal(out1, out2) and np.array_equal(lse1, lse2)
     rng = np.random.default_rng(9)
     perm = rng.permutation(w.num_blocks)
@@ -265,14 +307,15 @@ def test_rerun_and_page_permutation_are_bit_identical():
     cache2[perm] = w.cache
     w.cache = cache2
     w.block_table = perm[w.block_table].astype(np.int32)
-    out3, lse3, _ = run_gpu(w)
+    out3, lse3, _ = run_gpu(w, kernel=kernel)
     assert np.array_equal(out1, out3) and np.array_equal(lse1, lse3)
 
 
-def test_side_stream_and_graph_replay():
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_side_stream_and_graph_replay(kernel):
     w = I.dsv3_bf16(batch=4, seq_lo=200, seq_hi=900, num_segments=2)
     ref_o, ref_l = run_oracle(w)
-    dw = B.DeviceWorkload(w)
+    dw = B.DeviceWorkload(w, kernel=kernel)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
@@ -304,12 +347,15 @@ def _sampled(w, tokens, ns=None):
     return out[tokens], lse[tokens], ref_o, ref_l, dw
 
 
-def test_full_dsv3_bf16_sampled():
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_full_dsv3_bf16_sampled(kernel):
     w = I.dsv3_bf16()
     order = np.argsort(w.seq_lens)
     tokens = sorted({int(order[0]), int(order[-1]), 5, 31, 63})
-    out, lse, ro, rl, dw = _sampled(w, tokens)
-    assert_close(out, lse, ro, rl, "bf16", f"full dsv3 ns={dw.plan.num_segments}")
+    out, lse, dw = run_gpu(w, kernel=kernel)
+    ro, rl = run_oracle(w, tokens=tokens)
+    assert_close(out[tokens], lse[tokens], ro, rl, "bf16",
+                 f"full dsv3 ns={dw.plan.num_segments} k={kernel}")
 
 
 @pytest.mark.parametrize("heads", [16, 128])
