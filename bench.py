@@ -219,6 +219,23 @@ def cpu_baseline(budget_s=20.0):
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def aggregate_over_ranks(times_ms, units, device=None):
+    """Whole-job numbers from per-rank ones: every time is the max over ranks
+    (the slowest replica bounds the job), the work units are summed. Without
+    an initialised process group (one rank) the inputs come back unchanged."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return list(times_ms), float(units)
+    dev = device if device is not None else torch.device("cpu")
+    t = torch.tensor(list(times_ms), dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=dev)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return [float(x) for x in t.tolist()], float(u.item())
+
+
 def run_gpu(args):
     import numpy as np
     import torch
@@ -239,7 +256,10 @@ def run_gpu(args):
     BUILD.build()
     B.load_library()
     w = _workload(seed_offset=rank)
-    dw = B.DeviceWorkload(w, device=dev)
+    kern = {"auto": B.MLA_KERNEL_AUTO, "mma": B.MLA_KERNEL_WARP_MMA,
+            "tc": B.MLA_KERNEL_TCGEN05}[args.kernel]
+    dw = B.DeviceWorkload(w, device=dev, kernel=kern,
+                          num_segments=args.num_segments if args.num_segments else None)
     plan = dw.plan
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
@@ -328,19 +348,9 @@ def run_gpu(args):
         e2e_ms.append(e0.elapsed_time(e1))
 
     keys_rank = float(w.seq_lens.astype(np.int64).sum())
-    ms = statistics.mean(step_ms)
-    dms = statistics.mean(dec_ms)
-    ems = statistics.mean(e2e_ms)
-    if world > 1:
-        t = torch.tensor([ms, dms, ems, keys_rank], dtype=torch.float64, device=dev)
-        mx = t.clone()
-        dist.all_reduce(mx[:3], op=dist.ReduceOp.MAX)
-        ks = t[3:].clone()
-        dist.all_reduce(ks, op=dist.ReduceOp.SUM)
-        ms, dms, ems = (float(x) for x in mx[:3].tolist())
-        keys_total = float(ks.item())
-    else:
-        keys_total = keys_rank
+    (ms, dms, ems), keys_total = aggregate_over_ranks(
+        [statistics.mean(step_ms), statistics.mean(dec_ms), statistics.mean(e2e_ms)],
+        keys_rank, dev if world > 1 else None)
 
     if rank == 0:
         peaks, src = _peaks()
@@ -379,6 +389,7 @@ def run_gpu(args):
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ems},
             "gpu_launches": args.steps * (1 + (1 if NS > 1 else 0)),
+            "status_word": dw.status(),
             "wall_s_timed_region": wall,
         }
         if world == 1 and not args.no_cpu_baseline:
@@ -432,6 +443,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "tc"],
+                    help="decode kernel variant (default: the planner's choice)")
+    ap.add_argument("--num-segments", type=int, default=0,
+                    help="split-K segments (default: the planner's choice)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":

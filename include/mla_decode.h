@@ -103,8 +103,9 @@ typedef struct {
 typedef enum {
   MLA_KERNEL_AUTO = 0,
   MLA_KERNEL_WARP_MMA = 1,     /* warp-level MMA split-K kernel: every shape */
-  MLA_KERNEL_TCGEN05 = 2       /* tcgen05/TMEM CTA-pair kernel: dense bf16,
-                                  block_size a multiple of 64 */
+  MLA_KERNEL_TCGEN05 = 2       /* tcgen05/TMEM CTA-pair kernel: dense bf16 or
+                                  e4m3 with block_size a multiple of 64, or
+                                  sparse bf16 */
 } mla_kernel_t;
 
 /* Filled by mla_decode_plan; pass it unchanged to mla_decode_fwd or

@@ -157,7 +157,8 @@ mla_status_t launch_decode(const mla_plan_t* plan, const mla::DecodeParams& d, i
   if (plan->kernel == mla::kTcPair128) {
     const int64_t q_rows = static_cast<int64_t>(p.num_tokens) * p.num_heads;
     const int64_t kv_rows = static_cast<int64_t>(p.num_blocks) * p.block_size;
-    return cuda_status(mla::launch_decode_tc(d, q_rows, kv_rows, grid_of(plan), status, stream));
+    return cuda_status(mla::launch_decode_tc(d, p.kv_dtype == MLA_DTYPE_FP8_E4M3, q_rows, kv_rows,
+                                             grid_of(plan), status, stream));
   }
   return cuda_status(mla::launch_decode_mma(plan->kernel, p.kv_dtype == MLA_DTYPE_FP8_E4M3, d,
                                             grid_of(plan), stream));
@@ -202,7 +203,7 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   const bool sparse = p.topk > 0;
   const int32_t units = sparse ? p.num_tokens : p.num_reqs;
   const int64_t rows_per_unit = sparse ? p.num_heads : static_cast<int64_t>(p.num_heads) * p.max_qlen;
-  const bool tc_ok = !sparse && p.kv_dtype == MLA_DTYPE_BF16 && p.block_size % 64 == 0;
+  const bool tc_ok = sparse ? p.kv_dtype == MLA_DTYPE_BF16 : p.block_size % 64 == 0;
   if (p.kernel == MLA_KERNEL_TCGEN05 && !tc_ok) return MLA_ERR_UNSUPPORTED;
   const bool use_tc = tc_ok && p.kernel != MLA_KERNEL_WARP_MMA;
   int32_t kernel, rows;

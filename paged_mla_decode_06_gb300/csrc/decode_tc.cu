@@ -3,23 +3,26 @@
 // A CTA pair (thread-block cluster of 2) owns one (128-row tile, segment,
 // request). Rows are (token, head) pairs of the request; all of them share
 // one pass over each KV page. The 576 score columns and the 512 value
-// columns are split between the two CTAs so that neither re-reads the
-// other's bytes:
+// columns are split between the two CTAs so that neither loads the other's
+// bytes:
 //   CTA 0 loads cache columns [0, 256):   QK^T over dims [0, 256),   O[:, 0:256)
 //   CTA 1 loads cache columns [256, 576): QK^T over dims [256, 576), O[:, 256:512)
-// Per 64-key chunk (one TMA box of 64 rows x 64 columns per 128 bytes):
-//   TMA warp   -- loads this CTA's boxes of the page into a 2-stage ring
-//                 (block-table lookup per chunk, 128-byte swizzle);
-//   MMA thread -- S_c = Q_c K_c^T (M=128, N=64, bf16, fp32 in TMEM), and after
-//                 the softmax, O_c += P V_c (A = P in TMEM, B = V MN-major);
-//   softmax    -- 4 warps, one row per thread: read the partial scores from
-//                 TMEM, send them to the peer through distributed shared
-//                 memory, add the peer's partial, mask, base-2 online
-//                 softmax with a lazily updated reference max (O in TMEM is
-//                 rescaled only when the max grows by more than 2^8), write P
-//                 (bf16) back into TMEM over the scores.
+// Per 64-key chunk (one 128-byte-wide TMA box per 64 bf16 / 128 e4m3 columns):
+//   TMA warp   -- block-table lookup, this CTA's boxes of the page into a
+//                 STAGES-deep ring (128-byte swizzle);
+//   MMA thread -- S_c = Q_c K_c^T (M=128, N=64, fp32 in TMEM; kind::f16 for
+//                 bf16, kind::f8f6f4 for e4m3), then O_c += P V_c with P in
+//                 TMEM as the A operand and V an MN-major B operand (bf16, or
+//                 f16 for e4m3 caches);
+//   softmax    -- 4 warps, one row per thread: partial scores from TMEM, sent
+//                 to the peer through distributed shared memory, the peer's
+//                 partial added, masks, base-2 online softmax with a lazily
+//                 moved reference max (O in TMEM is rescaled only when the
+//                 max grows by more than 2^8), P written back into TMEM;
+//   convert    -- (e4m3 only) 4 warps widen the chunk's value columns to f16
+//                 in shared memory (exact), zeroing rows past the segment.
 // Both CTAs compute identical P, m and l (the same fp32 sum in either order).
-// TMEM: O at columns [0, 256), S/P double buffer at [256, 384).
+// TMEM: O at columns [0, 256), scores/P double buffer at [256, 384).
 // Every wait is bounded; on a timeout the kernel records an error code in
 // the status word, stops issuing work, drains what it issued and exits.
 #include <atomic>
@@ -38,37 +41,46 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 softmax
 constexpr int kRows = 128;
 constexpr int kKeys = 64;
-constexpr int kBoxQ = kRows * 128;     // 128 rows x 64 bf16 columns
-constexpr int kBoxKV = kKeys * 128;    // 64 rows x 64 bf16 columns
-constexpr int kMaxBoxes = 5;
-constexpr int kStages = 2;
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kMaxBoxes * kBoxQ;
+constexpr int kBoxQ = kRows * 128;     // 128 rows x 128 bytes
+constexpr int kBoxKV = kKeys * 128;    // 64 rows x 128 bytes
 constexpr int kRecvBytes = kRows * kKeys * 4;
-constexpr int kOffRecv = kOffKV + kStages * kMaxBoxes * kBoxKV;
-constexpr int kOffBar = kOffRecv + 2 * kRecvBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // barriers, TMEM slot, flags, 1 KB alignment
-static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-enum : int {
-  kQFull = 0, kKvFull = 1, kKvEmpty = 3, kSFull = 5, kPFull = 7, kRecvFull = 9, kPeerFree = 11,
-  kPvDone = 13, kOFinal = 15, kDrain = 16, kNumBars = 17
-};
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
+enum : int {
+  kQFull = 0, kKvFull = 1, kKvEmpty = 4, kSFull = 7, kPFull = 9, kRecvFull = 11,
+  kPeerFree = 13, kPvDone = 15, kOFinal = 17, kDrain = 18, kV16Full = 19, kNumBars = 20
+};
+
+template <bool FP8, bool SPARSE = false>
+struct Cfg {
+  static constexpr int kThreads = FP8 ? 320 : 192;  // + 4 conversion warps for e4m3
+  static constexpr int kBoxCols = FP8 ? 128 : 64;   // elements per 128-byte box row
+  static constexpr int kNbox0 = FP8 ? 2 : 4;        // CTA 0: columns [0, 256)
+  static constexpr int kNbox1 = FP8 ? 3 : 5;        // CTA 1: columns [256, 576 (+ zero fill))
+  static constexpr int kMaxBoxes = kNbox1;
+  static constexpr int kStages = FP8 ? 3 : 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kOffQ + kMaxBoxes * kBoxQ;
+  static constexpr int kOffV16 = kOffKV + kStages * kMaxBoxes * kBoxKV;
+  static constexpr int kV16Bytes = FP8 ? 4 * kBoxKV : 0;
+  static constexpr int kOffRecv = kOffV16 + kV16Bytes;
+  static constexpr int kOffBar = kOffRecv + 2 * kRecvBytes;
+  static constexpr int kSmem = kOffBar + 256 + 1024;  // barriers, TMEM slot, flag, alignment
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kStages <= 3, "barrier slots");
+};
+
 struct TcMaps {
-  CUtensorMap q;   // q viewed as [T*H rows, 576] bf16, box 64 x 128
-  CUtensorMap kv;  // cache viewed as [NB*BS rows, 576] bf16, box 64 x 64
+  CUtensorMap q;   // q viewed as [T*H rows, 576], box 128 bytes x 128 rows
+  CUtensorMap kv;  // cache viewed as [NB*BS rows, 576], box 128 bytes x 64 rows
 };
 
 struct Shared {
-  uint8_t* base;
   uint32_t bar0;
   volatile int* abort;
   __device__ uint32_t bar(int i) const { return bar0 + 8u * i; }
@@ -89,8 +101,9 @@ __device__ bool wait_phase(const Shared& sh, int* status, uint32_t bar, uint32_t
     if (*sh.abort) return false;
     if ((it & 63u) == 0) {
       const uint64_t now = global_timer_ns();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > kTimeoutNs) {
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kTimeoutNs) {
         report(status, code);
         *sh.abort = 1;
         return false;
@@ -99,13 +112,38 @@ __device__ bool wait_phase(const Shared& sh, int* status, uint32_t bar, uint32_t
   }
 }
 
+// Wait that ignores the abort flag (teardown drains), still bounded.
+__device__ void drain_wait(int* status, uint32_t bar, uint32_t parity, int code) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kTimeoutNs) {
+      report(status, code);
+      return;
+    }
+  }
+}
+
+template <bool F16>
+__device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
+  if constexpr (F16) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool FP8, bool SPARSE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ TcMaps maps, const DecodeParams p, int* status) {
+  using C = Cfg<FP8>;
+  static_assert(!(FP8 && SPARSE), "the sparse variant is bf16");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -119,12 +157,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int unit = blockIdx.z;
   const int H = p.num_heads;
 
-  int qlen = 1, tok0 = unit;
-  if (p.qo_indptr != nullptr) {
-    tok0 = p.qo_indptr[unit];
-    qlen = p.qo_indptr[unit + 1] - tok0;
+  int qlen = 1, tok0 = unit, part_len = 0;
+  int64_t list_base = 0;
+  if constexpr (SPARSE) {
+    if (p.slot_indptr != nullptr) {
+      list_base = p.slot_indptr[unit];
+      part_len = p.slot_indptr[unit + 1] - p.slot_indptr[unit];
+    } else {
+      list_base = static_cast<int64_t>(unit) * p.topk;
+      part_len = p.topk;
+    }
+  } else {
+    if (p.qo_indptr != nullptr) {
+      tok0 = p.qo_indptr[unit];
+      qlen = p.qo_indptr[unit + 1] - tok0;
+    }
+    part_len = p.seq_lens[unit];
   }
-  const int part_len = p.seq_lens[unit];
   const int rows_total = qlen * H;
   const int row0 = tile * kRows;
   if (row0 >= rows_total) return;  // both CTAs of the pair take this branch together
@@ -135,21 +184,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int seg_start = seg * seg_len;
   const int seg_end = min(seg_start + seg_len, part_len);
   const int n_chunks = seg_end > seg_start ? cdiv(seg_end - seg_start, kKeys) : 0;
-  const int nbox = crank == 0 ? 4 : 5;
+  const int nbox = crank == 0 ? C::kNbox0 : C::kNbox1;
   const int col0 = crank == 0 ? 0 : 256;
 
   Shared sh;
-  sh.base = smem;
-  sh.bar0 = smem_u32(smem + kOffBar);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffBar + 8 * kNumBars);
-  sh.abort = reinterpret_cast<volatile int*>(smem + kOffBar + 8 * kNumBars + 4);
+  sh.bar0 = smem_u32(smem + C::kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::kOffBar + 8 * kNumBars);
+  sh.abort = reinterpret_cast<volatile int*>(smem + C::kOffBar + 8 * kNumBars + 4);
 
   if (tid == 0) {
     *sh.abort = 0;
     mbar_init(sh.bar(kQFull), 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      // sparse: every lane of the gather warp arrives after its copies land
+      mbar_init(sh.bar(kKvFull + s), SPARSE ? 32 : 1);
+      // e4m3: the stage is free once QK^T (MMA commit) and the conversion
+      // warps (128 arrivals) have read it; bf16: once P.V has.
+      mbar_init(sh.bar(kKvEmpty + s), FP8 ? 129 : 1);
+    }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(sh.bar(kKvFull + b), 1);
-      mbar_init(sh.bar(kKvEmpty + b), 1);
       mbar_init(sh.bar(kSFull + b), 1);
       mbar_init(sh.bar(kPFull + b), 128);
       mbar_init(sh.bar(kRecvFull + b), 128);
@@ -158,6 +211,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(sh.bar(kOFinal), 1);
     mbar_init(sh.bar(kDrain), 1);
+    mbar_init(sh.bar(kV16Full), 128);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -170,7 +224,53 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   fence_after_sync();
   const uint32_t tbase = *tslot;
 
-  if (warp == 0) {
+  if (SPARSE && warp == 0) {
+    // ------------------------------------------------------------ row gather (sparse)
+    // Lane l copies rows 2l and 2l+1 of each chunk (this CTA's 128-byte column
+    // groups, swizzled like a TMA box); rows with no valid slot are skipped.
+    if (lane == 0) {
+      tma_prefetch_desc(&maps.q);
+      mbar_arrive_expect_tx(sh.bar(kQFull), nbox * kBoxQ);
+      for (int j = 0; j < nbox; ++j)
+        tma_load_2d(smem_u32(smem + C::kOffQ + j * kBoxQ), &maps.q, col0 + C::kBoxCols * j,
+                    tok0 * H + row0, sh.bar(kQFull));
+    }
+    const uint8_t* kvbytes = static_cast<const uint8_t*>(p.kv);
+    int c = 0;
+    for (; c < n_chunks; ++c) {
+      const int st = c % C::kStages;
+      if (c >= C::kStages) {
+        const bool okw = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kKvEmpty + st),
+                                                            (c / C::kStages - 1) & 1, false, 14));
+        if (!okw) break;
+      }
+      const int c0 = seg_start + c * kKeys;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int rr = 2 * lane + h;
+        const int pos = c0 + rr;
+        const int64_t slot = pos < seg_end ? static_cast<int64_t>(p.slots[list_base + pos]) : -1;
+        if (slot >= 0) {
+          const uint8_t* src = kvbytes + slot * (kHeadDim * 2) + col0 * 2;
+          const uint32_t dst = smem_u32(smem + C::kOffKV + (st * C::kMaxBoxes) * kBoxKV + rr * 128);
+          for (int j = 0; j < nbox; ++j)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              cp_async_16(dst + j * kBoxKV + ((k ^ (rr & 7)) << 4), src + j * 128 + k * 16, 16u);
+        }
+      }
+      cp_async_commit();
+      if (c >= 1) {
+        cp_async_wait<1>();
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        mbar_arrive(sh.bar(kKvFull + (c - 1) % C::kStages));
+      }
+    }
+    cp_async_wait<0>();
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    if (c >= 1) mbar_arrive(sh.bar(kKvFull + (c - 1) % C::kStages));
+    if (lane == 0) drain_wait(status, sh.bar(kQFull), 0, 13);
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&maps.q);
@@ -178,107 +278,96 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(sh.bar(kQFull), nbox * kBoxQ);
       const int qrow = tok0 * H + row0;
       for (int j = 0; j < nbox; ++j)
-        tma_load_2d(smem_u32(smem + kOffQ + j * kBoxQ), &maps.q, col0 + 64 * j, qrow,
+        tma_load_2d(smem_u32(smem + C::kOffQ + j * kBoxQ), &maps.q, col0 + C::kBoxCols * j, qrow,
                     sh.bar(kQFull));
       const int32_t* bt_row = p.block_table + static_cast<int64_t>(unit) * p.bt_stride;
       const int bs = p.block_size;
       int issued = 0;
       for (int c = 0; c < n_chunks; ++c) {
-        const int s = c & 1;
-        if (c >= 2 && !wait_phase(sh, status, sh.bar(kKvEmpty + s), ((c - 2) >> 1) & 1, false, 11))
+        const int st = c % C::kStages;
+        if (c >= C::kStages &&
+            !wait_phase(sh, status, sh.bar(kKvEmpty + st), (c / C::kStages - 1) & 1, false, 11))
           break;
         const int pos = seg_start + c * kKeys;
         const int blk = pos / bs;
         const int row = bt_row[blk] * bs + (pos - blk * bs);
-        mbar_arrive_expect_tx(sh.bar(kKvFull + s), nbox * kBoxKV);
+        mbar_arrive_expect_tx(sh.bar(kKvFull + st), nbox * kBoxKV);
         for (int j = 0; j < nbox; ++j)
-          tma_load_2d(smem_u32(smem + kOffKV + (s * kMaxBoxes + j) * kBoxKV), &maps.kv,
-                      col0 + 64 * j, row, sh.bar(kKvFull + s));
+          tma_load_2d(smem_u32(smem + C::kOffKV + (st * C::kMaxBoxes + j) * kBoxKV), &maps.kv,
+                      col0 + C::kBoxCols * j, row, sh.bar(kKvFull + st));
         issued = c + 1;
       }
-      // Drain: the last two loads issued must have landed before the CTA exits.
-      for (int c = max(0, issued - 2); c < issued; ++c) {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(sh.bar(kKvFull + (c & 1)), (c >> 1) & 1)) {
-          if (global_timer_ns() - t0 > kTimeoutNs) {
-            report(status, 12);
-            break;
-          }
-        }
-      }
-      {
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(sh.bar(kQFull), 0)) {
-          if (global_timer_ns() - t0 > kTimeoutNs) {
-            report(status, 13);
-            break;
-          }
-        }
-      }
+      // Drain: every load issued must have landed before the CTA exits.
+      for (int c = max(0, issued - C::kStages); c < issued; ++c)
+        drain_wait(status, sh.bar(kKvFull + c % C::kStages), (c / C::kStages) & 1, 12);
+      drain_wait(status, sh.bar(kQFull), 0, 13);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc_qk = instr_desc(kRows, kKeys, 1, 1, false, false);
-      const uint32_t idesc_pv = instr_desc(kRows, 256, 1, 1, false, true);
-      const uint32_t q_base = smem_u32(smem + kOffQ);
-      const uint32_t kv_base = smem_u32(smem + kOffKV);
+      const uint32_t idesc_qk = FP8 ? instr_desc(kRows, kKeys, 0, 0, false, false)
+                                    : instr_desc(kRows, kKeys, 1, 1, false, false);
+      const uint32_t idesc_pv = FP8 ? instr_desc(kRows, 256, 0, 0, false, true)
+                                    : instr_desc(kRows, 256, 1, 1, false, true);
+      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      const uint32_t kv_base = smem_u32(smem + C::kOffKV);
+      const uint32_t v16_base = smem_u32(smem + C::kOffV16);
       bool ok = n_chunks == 0 || wait_phase(sh, status, sh.bar(kQFull), 0, false, 21);
       auto issue_pv = [&](int cc) -> bool {
         const int b = cc & 1;
         if (!wait_phase(sh, status, sh.bar(kPFull + b), (cc >> 1) & 1, false, 22)) return false;
+        if (FP8 && !wait_phase(sh, status, sh.bar(kV16Full), cc & 1, false, 25)) return false;
         fence_after_sync();
-        const uint32_t v0 = kv_base + (b * kMaxBoxes) * kBoxKV;
+        const uint32_t v0 = FP8 ? v16_base : kv_base + ((cc % C::kStages) * C::kMaxBoxes) * kBoxKV;
 #pragma unroll
         for (int ks = 0; ks < kKeys / 16; ++ks) {
           const uint64_t bd = smem_desc_sw128(v0 + ks * 2048, kBoxKV, 1024);
           mma_ts(tbase + kTmemO, tbase + kTmemS + 64 * b + 8 * ks, bd, idesc_pv,
                  (cc | ks) != 0 ? 1u : 0u);
         }
-        mma_commit(sh.bar(kKvEmpty + b));
+        if (!FP8) mma_commit(sh.bar(kKvEmpty + cc % C::kStages));
         mma_commit(sh.bar(kPvDone + b));
         return true;
       };
       for (int c = 0; c < n_chunks && ok; ++c) {
         const int b = c & 1;
-        if (!wait_phase(sh, status, sh.bar(kKvFull + b), (c >> 1) & 1, false, 23)) {
+        const int st = c % C::kStages;
+        if (!wait_phase(sh, status, sh.bar(kKvFull + st), (c / C::kStages) & 1, false, 23)) {
           ok = false;
           break;
         }
         fence_after_sync();
-        const uint32_t kv0 = kv_base + (b * kMaxBoxes) * kBoxKV;
+        const uint32_t kv0 = kv_base + (st * C::kMaxBoxes) * kBoxKV;
         for (int j = 0; j < nbox; ++j) {
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint64_t ad = smem_desc_sw128(q_base + j * kBoxQ + k * 32, 16, 1024);
             const uint64_t bd = smem_desc_sw128(kv0 + j * kBoxKV + k * 32, 16, 1024);
-            mma_ss(tbase + kTmemS + 64 * b, ad, bd, idesc_qk, (j | k) != 0 ? 1u : 0u);
+            if constexpr (FP8)
+              mma_ss_f8(tbase + kTmemS + 64 * b, ad, bd, idesc_qk, (j | k) != 0 ? 1u : 0u);
+            else
+              mma_ss(tbase + kTmemS + 64 * b, ad, bd, idesc_qk, (j | k) != 0 ? 1u : 0u);
           }
         }
         mma_commit(sh.bar(kSFull + b));
+        if (FP8) mma_commit(sh.bar(kKvEmpty + st));
         if (c >= 1 && !issue_pv(c - 1)) ok = false;
       }
       if (ok && n_chunks >= 1 && issue_pv(n_chunks - 1)) mma_commit(sh.bar(kOFinal));
       // Drain every MMA this thread issued before TMEM is released.
       mma_commit(sh.bar(kDrain));
-      const uint64_t t0 = global_timer_ns();
-      while (!mbar_try_wait(sh.bar(kDrain), 0)) {
-        if (global_timer_ns() - t0 > kTimeoutNs) {
-          report(status, 24);
-          break;
-        }
-      }
+      drain_wait(status, sh.bar(kDrain), 0, 24);
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ softmax warps
     const int q4 = warp & 3;                 // TMEM lane quarter of this warp
     const int r = q4 * 32 + lane;            // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
     const int rho = row0 + r;
     const bool row_ok = rho < rows_total;
-    const int vis = row_ok ? part_len - qlen + rho / H + 1 : 0;
+    const int vis = !row_ok ? 0 : (SPARSE ? INT_MAX : part_len - qlen + rho / H + 1);
     const float scale2 = p.score_scale_log2;
-    const uint32_t recv_local = smem_u32(smem + kOffRecv);
+    const uint32_t recv_local = smem_u32(smem + C::kOffRecv);
     const uint32_t recv_peer = map_to_rank(recv_local, peer);
     const uint32_t bar_peer = map_to_rank(sh.bar0, peer);
     float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
@@ -306,7 +395,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive_cluster(bar_peer + 8u * (kRecvFull + b));
       ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kRecvFull + b), par, true, 33));
       if (!ok) break;
-      const uint8_t* src = smem + kOffRecv + b * kRecvBytes + r * 256;
+      const uint8_t* src = smem + C::kOffRecv + b * kRecvBytes + r * 256;
       float s[64];
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
@@ -318,13 +407,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       mbar_arrive_cluster(bar_peer + 8u * (kPeerFree + b));
 
-      // mask and chunk maximum
+      // keys of the chunk that exist: inside the segment and, for the sparse
+      // variant, with a valid slot (one ballot per 32 keys)
       const int c0 = seg_start + c * kKeys;
+      const int nvalid = min(kKeys, seg_end - c0);
+      uint64_t kmask = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+      if constexpr (SPARSE) {
+        const bool v0 = lane < nvalid && p.slots[list_base + c0 + lane] >= 0;
+        const bool v1 = lane + 32 < nvalid && p.slots[list_base + c0 + 32 + lane] >= 0;
+        kmask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
+                (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
+      }
+      // mask and chunk maximum
       const int lim = min(seg_end, vis) - c0;
       float mx = -INFINITY;
 #pragma unroll
       for (int j = 0; j < 64; ++j) {
-        s[j] = j < lim ? s[j] * scale2 : -INFINITY;
+        s[j] = (j < lim && ((kmask >> j) & 1ull)) ? s[j] * scale2 : -INFINITY;
         mx = fmaxf(mx, s[j]);
       }
       m_true = fmaxf(m_true, mx);
@@ -350,20 +449,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t o[64];
           tmem_ld_32x32b_x64(tbase + lane_off + kTmemO + 64 * g, o);
           tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 64; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
           uint32_t o0[32], o1[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            o0[j] = o[j];
-            o1[j] = o[32 + j];
+            o0[j] = __float_as_uint(__uint_as_float(o[j]) * alpha);
+            o1[j] = __float_as_uint(__uint_as_float(o[32 + j]) * alpha);
           }
           tmem_st_32x32b_x32(tbase + lane_off + kTmemO + 64 * g, o0);
           tmem_st_32x32b_x32(tbase + lane_off + kTmemO + 64 * g + 32, o1);
         }
         tmem_st_wait();
       }
-      // P = 2^(s - m_ref) as bf16, into TMEM over the scores
+      // P = 2^(s - m_ref), into TMEM over the scores
       const float base = m_ref == -INFINITY ? 0.f : m_ref;
       uint32_t pk[32];
       float ps = 0.f;
@@ -372,25 +469,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float p0 = fast_exp2(s[2 * j] - base);
         const float p1 = fast_exp2(s[2 * j + 1] - base);
         ps += p0 + p1;
-        pk[j] = pack_bf16(p0, p1);
+        pk[j] = pack_p<FP8>(p0, p1);
       }
       l += ps;
       tmem_st_32x32b_x32(tbase + lane_off + kTmemS + 64 * b, pk);
       tmem_st_wait();
-      // A partial last chunk: zero the value rows past the segment so that
-      // whatever the cache holds there cannot reach O through P = 0.
-      const int nvalid = seg_end - c0;
-      if (nvalid < kKeys) {
-        uint8_t* vbase = smem + kOffKV + (b * kMaxBoxes) * kBoxKV;
-        const int pieces = (kKeys - nvalid) * 8;  // 16-byte pieces per box
-        for (int i = tid - 64; i < 4 * pieces; i += 128) {
-          const int box = i / pieces;
-          const int rem = i - box * pieces;
-          const int row = nvalid + rem / 8;
-          *reinterpret_cast<uint4*>(vbase + box * kBoxKV + row * 128 + (rem & 7) * 16) =
-              make_uint4(0u, 0u, 0u, 0u);
+      if constexpr (!FP8) {
+        // Zero the value rows of keys that do not exist (past the segment, or
+        // an invalid sparse slot) so that whatever shared memory holds there
+        // cannot reach O through P = 0.
+        if (kmask != ~0ull) {
+          uint8_t* vbase = smem + C::kOffKV + ((c % C::kStages) * C::kMaxBoxes) * kBoxKV;
+          for (int i = tid - 64; i < 4 * kKeys * 8; i += 128) {
+            const int box = i >> 9;
+            const int row = (i >> 3) & 63;
+            if (!((kmask >> row) & 1ull))
+              *reinterpret_cast<uint4*>(vbase + box * kBoxKV + row * 128 + (i & 7) * 16) =
+                  make_uint4(0u, 0u, 0u, 0u);
+          }
+          asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         }
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       }
       fence_before_sync();
       mbar_arrive(sh.bar(kPFull + b));
@@ -465,9 +563,55 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if constexpr (FP8) {
+    // ------------------------------------------------------------ e4m3 -> f16 values
+    const int ct = tid - 192;  // 0..127
+    uint8_t* v16 = smem + C::kOffV16;
+    bool ok = true;
+    for (int c = 0; c < n_chunks && ok; ++c) {
+      const int st = c % C::kStages;
+      ok = __all_sync(0xffffffffu,
+                      wait_phase(sh, status, sh.bar(kKvFull + st), (c / C::kStages) & 1, false, 41));
+      if (!ok) break;
+      if (c >= 1) {
+        // the previous chunk's P.V has finished reading the f16 values
+        ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kPvDone + ((c - 1) & 1)),
+                                                 ((c - 1) >> 1) & 1, false, 42));
+        if (!ok) break;
+      }
+      const int nvalid = min(kKeys, seg_end - (seg_start + c * kKeys));
+      const uint8_t* src = smem + C::kOffKV + (st * C::kMaxBoxes) * kBoxKV;
+      // boxes 0 and 1 of the stage hold this CTA's 256 value columns
+      for (int i = ct; i < 2 * kKeys * 8; i += 128) {
+        const int box = i >> 9;
+        const int rem = i & 511;
+        const int row = rem >> 3;
+        const int k = rem & 7;  // logical 16-byte chunk (16 e4m3 values)
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (row < nvalid)
+          v = *reinterpret_cast<const uint4*>(src + box * kBoxKV + row * 128 + ((k ^ (row & 7)) << 4));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t h[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          h[2 * e] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[e] & 0xFFFF));
+          h[2 * e + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[e] >> 16));
+        }
+        const int dbox = box * 2 + (k >> 2);
+        const int lc = (k & 3) * 2;
+        uint8_t* drow = v16 + dbox * kBoxKV + row * 128;
+        *reinterpret_cast<uint4*>(drow + ((lc ^ (row & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+        *reinterpret_cast<uint4*>(drow + (((lc + 1) ^ (row & 7)) << 4)) =
+            make_uint4(h[4], h[5], h[6], h[7]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      mbar_arrive(sh.bar(kKvEmpty + st));
+      mbar_arrive(sh.bar(kV16Full));
+    }
   }
 
   // ------------------------------------------------------------ teardown
+  __syncwarp();
   fence_before_sync();
   __syncthreads();
   cluster_sync();  // no remote access to this CTA's shared memory after here
@@ -490,42 +634,58 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+// 2-D map over a [rows, 576] tensor with 128-byte-wide boxes of box_rows rows.
+cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool fp8) {
   auto enc = encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
+  const uint32_t elt = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * elt};
+  cuuint32_t box[2] = {128 / elt, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <bool FP8, bool SPARSE>
+cudaError_t launch_variant(const TcMaps& maps, const DecodeParams& p, dim3 grid, int* status,
+                           cudaStream_t stream) {
+  using C = Cfg<FP8>;
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(decode_tc_kernel<FP8, SPARSE>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  decode_tc_kernel<FP8, SPARSE><<<grid, C::kThreads, C::kSmem, stream>>>(maps, p, status);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
-int decode_tc_smem_bytes() { return kSmemBytes; }
+int decode_tc_smem_bytes(bool fp8) { return fp8 ? Cfg<true>::kSmem : Cfg<false>::kSmem; }
 
-cudaError_t launch_decode_tc(const DecodeParams& p, int64_t q_rows, int64_t kv_rows, dim3 grid,
-                             int* status, cudaStream_t stream) {
+cudaError_t launch_decode_tc(const DecodeParams& p, bool fp8, int64_t q_rows, int64_t kv_rows,
+                             dim3 grid, int* status, cudaStream_t stream) {
   TcMaps maps;
-  cudaError_t e = make_map(&maps.q, p.q, static_cast<uint64_t>(q_rows), kRows);
+  cudaError_t e = make_map(&maps.q, p.q, static_cast<uint64_t>(q_rows), kRows, fp8);
   if (e != cudaSuccess) return e;
-  e = make_map(&maps.kv, p.kv, static_cast<uint64_t>(kv_rows), kKeys);
+  e = make_map(&maps.kv, p.kv, static_cast<uint64_t>(kv_rows), kKeys, fp8);
   if (e != cudaSuccess) return e;
-  static std::atomic<uint64_t> done{0};
-  int dev = 0;
-  e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(done.load(std::memory_order_acquire) & bit)) {
-    e = cudaFuncSetAttribute(decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    done.fetch_or(bit, std::memory_order_acq_rel);
+  if (p.slots != nullptr) {
+    if (fp8) return cudaErrorNotSupported;
+    return launch_variant<false, true>(maps, p, grid, status, stream);
   }
-  decode_tc_kernel<<<grid, kThreads, kSmemBytes, stream>>>(maps, p, status);
-  return cudaGetLastError();
+  return fp8 ? launch_variant<true, false>(maps, p, grid, status, stream)
+             : launch_variant<false, false>(maps, p, grid, status, stream);
 }
 
 }  // namespace mla

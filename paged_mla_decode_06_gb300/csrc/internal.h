@@ -71,11 +71,11 @@ cudaError_t launch_index_convert(const int32_t* req_id, const int32_t* block_tab
 // tcgen05 CTA-pair kernel: q_rows / kv_rows are the row counts of the q
 // and cache tensors viewed as [rows, 576]; status (may be null) receives a
 // nonzero code if a bounded wait times out.
-cudaError_t launch_decode_tc(const DecodeParams& p, int64_t q_rows, int64_t kv_rows, dim3 grid,
-                             int* status, cudaStream_t stream);
+cudaError_t launch_decode_tc(const DecodeParams& p, bool fp8, int64_t q_rows, int64_t kv_rows,
+                             dim3 grid, int* status, cudaStream_t stream);
 
 // Shared memory bytes a decode variant needs (host query for validation).
 int decode_mma_smem_bytes(int32_t kernel, bool fp8);
-int decode_tc_smem_bytes();
+int decode_tc_smem_bytes(bool fp8);
 
 }  // namespace mla
