@@ -53,9 +53,9 @@ def _peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def _workload(seed_offset=0):
+def _workload(seed_offset=0, batch=64):
     from paged_mla_decode_06_gb300 import inputs as I
-    return I.dsv3_bf16(seed=2 + seed_offset)
+    return I.dsv3_bf16(seed=2 + seed_offset, batch=batch)
 
 
 def _flops(w):
@@ -255,7 +255,7 @@ def run_gpu(args):
 
     BUILD.build()
     B.load_library()
-    w = _workload(seed_offset=rank)
+    w = _workload(seed_offset=rank, batch=args.batch)
     kern = {"auto": B.MLA_KERNEL_AUTO, "mma": B.MLA_KERNEL_WARP_MMA,
             "tc": B.MLA_KERNEL_TCGEN05}[args.kernel]
     dw = B.DeviceWorkload(w, device=dev, kernel=kern,
@@ -358,6 +358,8 @@ def run_gpu(args):
         achieved = alg / (dms * 1e-3) / 1e9
         peak_bw = float(peaks["hbm_gbs"])
         tflops = _flops(w) / (dms * 1e-3) / 1e12
+        workload = WORKLOAD if args.batch == 64 else WORKLOAD.replace("batch 64",
+                                                                        f"batch {args.batch}")
         line = {
             "metric": METRIC,
             "value": keys_total / (ms * 1e-3),
@@ -372,7 +374,7 @@ def run_gpu(args):
             "vs_baseline": None,
             "dtype": "bf16",
             "data": "synthetic (seeded numpy; no dataset or weights)",
-            "config": {"workload": WORKLOAD, "num_segments": NS, "tile_size": plan.tile_size,
+            "config": {"workload": workload, "num_segments": NS, "tile_size": plan.tile_size,
                        "rows_per_cta": plan.rows_per_cta, "kernel": int(plan.kernel),
                        "kv_tokens_per_gpu": int(keys_rank),
                        "l2": "flushed (256 MiB write) before every timed step",
@@ -447,6 +449,9 @@ def main():
                     help="decode kernel variant (default: the planner's choice)")
     ap.add_argument("--num-segments", type=int, default=0,
                     help="split-K segments (default: the planner's choice)")
+    ap.add_argument("--batch", type=int, default=64,
+                    help="requests per batch (64 is the measured workload; smaller batches "
+                         "of the same shape are for profiler captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":

@@ -49,11 +49,13 @@ constexpr int kRecvBytes = kRows * kKeys * 4;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;
 constexpr uint32_t kTmemS = 256;
+constexpr uint32_t kTmemQ = 384;  // bf16: q of the CTA's 256 latent dims (A operand of QK^T)
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
 enum : int {
   kQFull = 0, kKvFull = 1, kKvEmpty = 4, kSFull = 7, kPFull = 9, kRecvFull = 11,
-  kPeerFree = 13, kPvDone = 15, kOFinal = 17, kDrain = 18, kV16Full = 19, kNumBars = 20
+  kPeerFree = 13, kPvDone = 15, kOFinal = 17, kDrain = 18, kV16Full = 19, kQTmem = 20,
+  kNumBars = 21
 };
 
 template <bool FP8, bool SPARSE = false>
@@ -63,9 +65,12 @@ struct Cfg {
   static constexpr int kNbox0 = FP8 ? 2 : 4;        // CTA 0: columns [0, 256)
   static constexpr int kNbox1 = FP8 ? 3 : 5;        // CTA 1: columns [256, 576 (+ zero fill))
   static constexpr int kMaxBoxes = kNbox1;
-  static constexpr int kStages = FP8 ? 3 : 2;
+  // bf16 keeps q's 256 latent dims in TMEM and only CTA 1's rope box in
+  // shared memory; e4m3 keeps all of q in shared memory.
+  static constexpr int kQSmemBoxes = FP8 ? kNbox1 : 1;
+  static constexpr int kStages = 3;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kOffQ + kMaxBoxes * kBoxQ;
+  static constexpr int kOffKV = kOffQ + kQSmemBoxes * kBoxQ;
   static constexpr int kOffV16 = kOffKV + kStages * kMaxBoxes * kBoxKV;
   static constexpr int kV16Bytes = FP8 ? 4 * kBoxKV : 0;
   static constexpr int kOffRecv = kOffV16 + kV16Bytes;
@@ -137,6 +142,24 @@ __device__ __forceinline__ uint32_t pack_p(float lo, float hi) {
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// The part of q that lives in shared memory: every box for e4m3; for bf16
+// only CTA 1's rope box (x = 512), CTA 0 has none and just arrives.
+template <bool FP8>
+__device__ void load_q_smem(const TcMaps& maps, uint8_t* dst, uint32_t bar, uint32_t crank,
+                            int nbox, int col0, int qrow) {
+  tma_prefetch_desc(&maps.q);
+  if constexpr (FP8) {
+    mbar_arrive_expect_tx(bar, nbox * kBoxQ);
+    for (int j = 0; j < nbox; ++j)
+      tma_load_2d(smem_u32(dst + j * kBoxQ), &maps.q, col0 + 128 * j, qrow, bar);
+  } else if (crank == 1) {
+    mbar_arrive_expect_tx(bar, kBoxQ);
+    tma_load_2d(smem_u32(dst), &maps.q, 512, qrow, bar);
+  } else {
+    mbar_arrive(bar);
+  }
 }
 
 template <bool FP8, bool SPARSE>
@@ -212,6 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
     mbar_init(sh.bar(kOFinal), 1);
     mbar_init(sh.bar(kDrain), 1);
     mbar_init(sh.bar(kV16Full), 128);
+    mbar_init(sh.bar(kQTmem), 128);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -228,13 +252,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
     // ------------------------------------------------------------ row gather (sparse)
     // Lane l copies rows 2l and 2l+1 of each chunk (this CTA's 128-byte column
     // groups, swizzled like a TMA box); rows with no valid slot are skipped.
-    if (lane == 0) {
-      tma_prefetch_desc(&maps.q);
-      mbar_arrive_expect_tx(sh.bar(kQFull), nbox * kBoxQ);
-      for (int j = 0; j < nbox; ++j)
-        tma_load_2d(smem_u32(smem + C::kOffQ + j * kBoxQ), &maps.q, col0 + C::kBoxCols * j,
-                    tok0 * H + row0, sh.bar(kQFull));
-    }
+    if (lane == 0) load_q_smem<FP8>(maps, smem + C::kOffQ, sh.bar(kQFull), crank, nbox, col0,
+                                    tok0 * H + row0);
     const uint8_t* kvbytes = static_cast<const uint8_t*>(p.kv);
     int c = 0;
     for (; c < n_chunks; ++c) {
@@ -273,13 +292,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
   } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&maps.q);
       tma_prefetch_desc(&maps.kv);
-      mbar_arrive_expect_tx(sh.bar(kQFull), nbox * kBoxQ);
-      const int qrow = tok0 * H + row0;
-      for (int j = 0; j < nbox; ++j)
-        tma_load_2d(smem_u32(smem + C::kOffQ + j * kBoxQ), &maps.q, col0 + C::kBoxCols * j, qrow,
-                    sh.bar(kQFull));
+      load_q_smem<FP8>(maps, smem + C::kOffQ, sh.bar(kQFull), crank, nbox, col0, tok0 * H + row0);
       const int32_t* bt_row = p.block_table + static_cast<int64_t>(unit) * p.bt_stride;
       const int bs = p.block_size;
       int issued = 0;
@@ -313,6 +327,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
       const uint32_t kv_base = smem_u32(smem + C::kOffKV);
       const uint32_t v16_base = smem_u32(smem + C::kOffV16);
       bool ok = n_chunks == 0 || wait_phase(sh, status, sh.bar(kQFull), 0, false, 21);
+      if (!FP8 && ok && n_chunks > 0) ok = wait_phase(sh, status, sh.bar(kQTmem), 0, false, 26);
       auto issue_pv = [&](int cc) -> bool {
         const int b = cc & 1;
         if (!wait_phase(sh, status, sh.bar(kPFull + b), (cc >> 1) & 1, false, 22)) return false;
@@ -338,15 +353,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
         }
         fence_after_sync();
         const uint32_t kv0 = kv_base + (st * C::kMaxBoxes) * kBoxKV;
-        for (int j = 0; j < nbox; ++j) {
+        if constexpr (FP8) {
+          for (int j = 0; j < nbox; ++j) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const uint64_t ad = smem_desc_sw128(q_base + j * kBoxQ + k * 32, 16, 1024);
-            const uint64_t bd = smem_desc_sw128(kv0 + j * kBoxKV + k * 32, 16, 1024);
-            if constexpr (FP8)
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc_sw128(q_base + j * kBoxQ + k * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(kv0 + j * kBoxKV + k * 32, 16, 1024);
               mma_ss_f8(tbase + kTmemS + 64 * b, ad, bd, idesc_qk, (j | k) != 0 ? 1u : 0u);
-            else
-              mma_ss(tbase + kTmemS + 64 * b, ad, bd, idesc_qk, (j | k) != 0 ? 1u : 0u);
+            }
+          }
+        } else {
+          // 256 latent dims: A = q in TMEM (8 columns per 16 dims)
+          for (int j = 0; j < 4; ++j) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t bd = smem_desc_sw128(kv0 + j * kBoxKV + k * 32, 16, 1024);
+              mma_ts(tbase + kTmemS + 64 * b, tbase + kTmemQ + 32 * j + 8 * k, bd, idesc_qk,
+                     (j | k) != 0 ? 1u : 0u);
+            }
+          }
+          if (crank == 1) {  // 64 rope dims: A = q's rope box in shared memory
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t ad = smem_desc_sw128(q_base + k * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(kv0 + 4 * kBoxKV + k * 32, 16, 1024);
+              mma_ss(tbase + kTmemS + 64 * b, ad, bd, idesc_qk, 1u);
+            }
           }
         }
         mma_commit(sh.bar(kSFull + b));
@@ -371,6 +403,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
     const uint32_t recv_peer = map_to_rank(recv_local, peer);
     const uint32_t bar_peer = map_to_rank(sh.bar0, peer);
     float m_ref = -INFINITY, m_true = -INFINITY, l = 0.f;
+    if constexpr (!FP8) {
+      // this row's 256 latent dims of q into TMEM (packed bf16 pairs)
+      const int64_t qrow = static_cast<int64_t>(tok0) * H + row0 + r;
+      const bool qok = qrow < static_cast<int64_t>(p.num_tokens) * H;
+      const uint4* qsrc = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                         (qok ? qrow : 0) * kHeadDim + col0);
+#pragma unroll 1
+      for (int g = 0; g < 4; ++g) {
+        uint32_t v[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint4 x = qok ? __ldg(qsrc + 8 * g + i) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * i] = x.x;
+          v[4 * i + 1] = x.y;
+          v[4 * i + 2] = x.z;
+          v[4 * i + 3] = x.w;
+        }
+        tmem_st_32x32b_x32(tbase + lane_off + kTmemQ + 32 * g, v);
+      }
+      tmem_st_wait();
+      fence_before_sync();
+      mbar_arrive(sh.bar(kQTmem));
+    }
     bool ok = true;
     for (int c = 0; c < n_chunks && ok; ++c) {
       const int b = c & 1;

@@ -212,10 +212,11 @@ def test_tcgen05_segment_partials():
     assert np.max(np.abs(so - ro)) < 1e-2
 
 
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("heads", [16, 32, 48, 64, 96, 128])
-def test_fp8_heads(heads):
-    w = I.fp8_decode(heads, batch=3, seq_len=2048)
-    out, lse, _ = run_gpu(w)
+def test_fp8_heads(heads, kernel):
+    w = I.fp8_decode(heads, batch=3, seq_len=2048, num_segments=2)
+    out, lse, _ = run_gpu(w, kernel=kernel)
     ref_o, ref_l = run_oracle(w)
     assert_close(out, lse, ref_o, ref_l, "fp8", f"fp8 H={heads}")
 
@@ -265,23 +266,25 @@ def test_multi_token_rows_and_short_sequences():
 
 # ---------------------------------------------------------------- sparse decode
 
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 @pytest.mark.parametrize("ns", [0, 1, 4])
-def test_sparse_small(ns):
+def test_sparse_small(ns, kernel):
     w = I.sparse_topk(num_reqs=3, tokens_per_req=4, cache_tokens=4096, topk=512,
                       interspersed_rows=2, max_pad=64, num_segments=ns)
-    out, lse, dw = run_gpu(w)
+    out, lse, dw = run_gpu(w, kernel=kernel)
     assert np.array_equal(dw.slots.cpu().numpy().astype(np.int64), oracle_slots(w))
     ref_o, ref_l = run_oracle(w)
     assert_close(out, lse, ref_o, ref_l, "bf16", "sparse")
 
 
-def test_sparse_ragged_indptr():
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+def test_sparse_ragged_indptr(kernel):
     w = I.sparse_topk(num_reqs=2, tokens_per_req=3, cache_tokens=2048, topk=256, max_pad=0)
     slots = oracle_slots(w)
     lens = np.array([256, 0, 17, 128, 255, 1])
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
     flat = np.concatenate([slots[t, :lens[t]] for t in range(6)]).astype(np.int32)
-    dw = B.DeviceWorkload(w, num_segments=3)
+    dw = B.DeviceWorkload(w, num_segments=3, kernel=kernel)
     dev = dw.device
     B.mla_decode_fwd(dw.plan, dw.q, dw.cache, sparse_slots=torch.from_numpy(flat).to(dev),
                      sparse_indptr=torch.from_numpy(cu).to(dev), softmax_scale=w.softmax_scale,
@@ -289,6 +292,7 @@ def test_sparse_ragged_indptr():
     torch.cuda.synchronize()
     ref_o, ref_l = O.mla_decode(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, None, None,
                                 w.softmax_scale, sparse_slots=flat, sparse_indptr=cu)
+    assert dw.status() == 0
     assert_close(dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), ref_o, ref_l, "bf16",
                  "sparse ragged")
 
