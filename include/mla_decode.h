@@ -253,6 +253,26 @@ MLA_API mla_status_t mla_sparse_index_convert(const int32_t* req_id, const int32
                                       const int32_t* cu_seqlens, int32_t* out,
                                       cudaStream_t stream);
 
+/*
+ * mla_merge_lse -- combine the (out, lse) of W key shards of the same rows,
+ * the cross-rank merge that consumes the natural-log LSE of
+ * mla_decode_fwd / mla_merge_segments under decode context parallelism
+ * ([merge] module docstring: "the natural-log LSE it returns is what the
+ * cross-rank DCP merge consumes"). With M = max_w lse_w:
+ *   out = sum_w e^(lse_w - M) out_w / Z,  lse = M + ln Z,
+ *   Z = sum_w e^(lse_w - M) (+ e^(sink - M)).
+ * Shards with lse = -inf take no part; no shard and no sink gives out = 0,
+ * lse = -inf. A sink is folded here once, so shards are decoded without it.
+ *   shard_out [W, T, H, kv_lora_rank] bf16, shard_lse [W, T, H] fp32,
+ *   sinks [H] fp32 or NULL, out [T, H, kv_lora_rank] bf16, lse [T, H] fp32.
+ * kv_lora_rank must be 128, 256 or 512.
+ * Errors: MLA_ERR_INVALID_ARG, MLA_ERR_CUDA.
+ */
+MLA_API mla_status_t mla_merge_lse(const void* shard_out, const float* shard_lse,
+                                   int32_t num_shards, int32_t num_tokens, int32_t num_heads,
+                                   int32_t kv_lora_rank, const float* sinks, void* out,
+                                   float* lse, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 MLA_API const char* mla_status_string(mla_status_t status);
 

@@ -380,3 +380,56 @@ def index_convert(req_id, block_table, token_indices, block_size, cu_seqlens=Non
         n = int(cu[t + 1] - cu[t])
         out[cu[t]:cu[t] + n] = conv[t, :n]
     return out
+
+
+# ---------------------------------------------------------------------------
+# merge of per-shard (out, lse) pairs (decode context parallelism)
+# ---------------------------------------------------------------------------
+
+def merge_lse_shards(outs, lses, sinks=None):
+    """Combine the natural-log ``(out, lse)`` of W key shards of the same rows.
+
+    The merge page says its natural-log LSE is what the cross-rank DCP merge
+    consumes; with shard ``w`` holding ``out_w = sum_p e^{s_p} v_p / Z_w`` and
+    ``lse_w = ln Z_w`` over its own keys: ``M = max_w lse_w``,
+    ``out = sum_w e^{lse_w - M} out_w / sum_w e^{lse_w - M}``,
+    ``lse = M + ln sum_w e^{lse_w - M}``. Shards with ``lse = -inf`` (no keys)
+    take no part. A sink, if given, is folded once here (it adds
+    ``e^{sink - M}`` to the denominator), so the shards must be decoded
+    without it. ``outs [W, T, H, Dv]``, ``lses [W, T, H]``.
+    """
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    W, T, H, DV = outs.shape
+    out = np.zeros((T, H, DV))
+    lse = np.full((T, H), -np.inf)
+    sk = None if sinks is None else np.asarray(sinks, dtype=np.float64)
+    for t in range(T):
+        for h in range(H):
+            live = [w for w in range(W) if lses[w, t, h] > -np.inf]
+            cands = [lses[w, t, h] for w in live]
+            if sk is not None:
+                cands.append(sk[h])
+            if not cands:
+                continue
+            M = max(cands)
+            Z = 0.0
+            acc = np.zeros(DV)
+            for w in live:
+                e = math.exp(lses[w, t, h] - M)
+                Z += e
+                acc += e * outs[w, t, h]
+            if sk is not None:
+                Z += math.exp(sk[h] - M)
+            out[t, h] = acc / Z
+            lse[t, h] = M + math.log(Z)
+    return out, lse
+
+
+def round_robin_positions(seq_len: int, qlen: int, j: int, world: int, rank: int):
+    """Logical positions a rank holds of row ``j``'s visible keys when token
+    ``p`` lives on rank ``p % world`` (decode context parallelism with an
+    interleave of one): ``{p < visible_len(seq_len, qlen, j) : p % world == rank}``
+    (``dcp_local_verify_row_lens`` counts exactly these)."""
+    n = visible_len(seq_len, qlen, j)
+    return np.arange(rank, n, world, dtype=np.int64)

@@ -97,6 +97,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                  _vp, _vp, _vp]
         lib.mla_sparse_index_convert.restype = st
+        lib.mla_merge_lse.argtypes = [_vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, _vp, _vp, _vp, _vp]
+        lib.mla_merge_lse.restype = st
         lib.mla_status_string.argtypes = [ctypes.c_int32]
         lib.mla_status_string.restype = ctypes.c_char_p
         lib.mla_last_cuda_error.argtypes = []
@@ -201,6 +204,14 @@ def mla_merge_segments(segm_output, segm_max, segm_expsum, part_lens, *, tile_si
     _check("mla_merge_segments", lib.mla_merge_segments(
         _ptr(segm_output), _ptr(segm_max), _ptr(segm_expsum), _ptr(part_lens), T, H, NS, rank,
         int(tile_size), _ptr(sinks), MLA_DTYPE_BF16, _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def mla_merge_lse(shard_out, shard_lse, *, sinks=None, out, lse, stream=None) -> None:
+    lib = load_library()
+    W, T, H, rank = shard_out.shape
+    _check("mla_merge_lse", lib.mla_merge_lse(
+        _ptr(shard_out), _ptr(shard_lse), W, T, H, rank, _ptr(sinks), _ptr(out), _ptr(lse),
+        _stream(stream)))
 
 
 def mla_sparse_index_convert(req_id, block_table, token_indices, *, block_size: int,

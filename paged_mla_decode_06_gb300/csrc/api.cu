@@ -368,6 +368,30 @@ mla_status_t mla_merge_segments(const float* segm_output, const float* segm_max,
   return cuda_status(mla::launch_merge(m, stream));
 }
 
+mla_status_t mla_merge_lse(const void* shard_out, const float* shard_lse, int32_t num_shards,
+                           int32_t num_tokens, int32_t num_heads, int32_t kv_lora_rank,
+                           const float* sinks, void* out, float* lse, cudaStream_t stream) {
+  if (num_shards < 1 || num_tokens < 0 || num_heads <= 0) return MLA_ERR_INVALID_ARG;
+  if (kv_lora_rank != 128 && kv_lora_rank != 256 && kv_lora_rank != 512) return MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MLA_OK;
+  if (shard_out == nullptr || shard_lse == nullptr || out == nullptr || lse == nullptr)
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned(shard_out, 16) || !aligned(out, 16) || !aligned(shard_lse, 4) || !aligned(lse, 4) ||
+      (sinks != nullptr && !aligned(sinks, 4)))
+    return MLA_ERR_INVALID_ARG;
+  mla::LseMergeParams m{};
+  m.shard_out = shard_out;
+  m.shard_lse = shard_lse;
+  m.num_shards = num_shards;
+  m.num_tokens = num_tokens;
+  m.num_heads = num_heads;
+  m.rank = kv_lora_rank;
+  m.sinks = sinks;
+  m.out = out;
+  m.lse = lse;
+  return cuda_status(mla::launch_merge_lse(m, stream));
+}
+
 mla_status_t mla_sparse_index_convert(const int32_t* req_id, const int32_t* block_table,
                                       int32_t bt_rows, int32_t bt_cols, int64_t bt_row_stride,
                                       const int32_t* token_indices, int64_t ti_row_stride,

@@ -59,6 +59,16 @@ struct MergeParams {
   float* lse;
 };
 
+struct LseMergeParams {
+  const void* shard_out;   // [W, T, H, rank] bf16
+  const float* shard_lse;  // [W, T, H] natural log
+  int32_t num_shards, num_tokens, num_heads, rank;
+  const float* sinks;      // [H] or null
+  void* out;               // [T, H, rank] bf16
+  float* lse;              // [T, H]
+};
+
+cudaError_t launch_merge_lse(const LseMergeParams& p, cudaStream_t stream);
 cudaError_t launch_decode_mma(int32_t kernel, bool fp8, const DecodeParams& p, dim3 grid,
                               cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);

@@ -98,7 +98,77 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
   if (lane == 0) p.lse[gw] = kLn2 * (M + log2f(W));
 }
 
+// Natural-log (out, lse) pairs of W key shards of the same rows: weights
+// e^(lse_w - M), one warp per (token, head), bf16 shard outputs read 8 bytes
+// per lane per step (coalesced).
+template <int VPL>
+__global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_lse_kernel(const LseMergeParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int64_t rows = static_cast<int64_t>(p.num_tokens) * p.num_heads;
+  if (gw >= rows) return;
+  const int h = static_cast<int>(gw % p.num_heads);
+  float M = -INFINITY;
+  for (int w = 0; w < p.num_shards; ++w) M = fmaxf(M, p.shard_lse[w * rows + gw]);
+  const bool has_sink = p.sinks != nullptr;
+  const float sink = has_sink ? p.sinks[h] : -INFINITY;
+  M = fmaxf(M, sink);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + gw * p.rank;
+  if (M == -INFINITY) {
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+      *reinterpret_cast<uint2*>(out + (v * 32 + lane) * 4) = make_uint2(0u, 0u);
+    if (lane == 0) p.lse[gw] = -INFINITY;
+    return;
+  }
+  float acc[VPL][4];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
+  float Z = 0.f;
+  for (int w = 0; w < p.num_shards; ++w) {
+    const float l = p.shard_lse[w * rows + gw];
+    if (l == -INFINITY) continue;
+    const float e = expf(l - M);
+    Z += e;
+    const uint2* src = reinterpret_cast<const uint2*>(
+        static_cast<const __nv_bfloat16*>(p.shard_out) + (w * rows + gw) * p.rank);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) {
+      const uint2 x = __ldg(src + v * 32 + lane);
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.x));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&x.y));
+      acc[v][0] += e * a.x;
+      acc[v][1] += e * a.y;
+      acc[v][2] += e * b.x;
+      acc[v][3] += e * b.y;
+    }
+  }
+  if (has_sink) Z += expf(sink - M);
+  const float inv = 1.f / Z;
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[v][0] * inv, acc[v][1] * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[v][2] * inv, acc[v][3] * inv);
+    *reinterpret_cast<uint2*>(out + (v * 32 + lane) * 4) =
+        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+  if (lane == 0) p.lse[gw] = M + logf(Z);
+}
+
 }  // namespace
+
+cudaError_t launch_merge_lse(const LseMergeParams& p, cudaStream_t stream) {
+  const int64_t warps = static_cast<int64_t>(p.num_tokens) * p.num_heads;
+  if (warps == 0) return cudaSuccess;
+  const unsigned blocks = static_cast<unsigned>((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  switch (p.rank / 128) {
+    case 1: merge_lse_kernel<1><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(p); break;
+    case 2: merge_lse_kernel<2><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(p); break;
+    case 4: merge_lse_kernel<4><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(p); break;
+    default: return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
 
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t warps = static_cast<int64_t>(p.num_tokens) * p.num_heads;

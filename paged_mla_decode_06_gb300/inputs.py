@@ -338,3 +338,20 @@ def sparse_topk(seed: int = 5, num_reqs: int = 16, tokens_per_req: int = 8,
                         max_pad=max_pad, interspersed_rows=interspersed_rows,
                         num_segments=num_segments,
                         name=f"sparse_r{num_reqs}x{tokens_per_req}_h{num_heads}_k{topk}")
+
+
+def dcp_shard_positions(w: Workload, world: int, rank: int, pad_to: int = 128):
+    """Per-token logical positions one rank holds when token ``p`` of a
+    request lives on rank ``p % world`` (decode context parallelism, interleave
+    1), for single-token rows: ``[T, K]`` int32, -1 padded to a multiple of
+    ``pad_to``, plus the request id of every token."""
+    if w.qo_indptr is not None:
+        raise ValueError("shard positions are built for one token per request")
+    T = w.num_tokens
+    lists = [np.arange(rank, int(w.seq_lens[t]), world, dtype=np.int32) for t in range(T)]
+    K = max([len(l) for l in lists] + [1])
+    K = -(-K // pad_to) * pad_to
+    idx = np.full((T, K), -1, dtype=np.int32)
+    for t, l in enumerate(lists):
+        idx[t, :len(l)] = l
+    return idx, np.arange(T, dtype=np.int32)

@@ -214,3 +214,12 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(B, "_lib", None)
     with pytest.raises(RuntimeError, match="not found"):
         B.load_library(str(tmp_path / "nope.so"))
+
+
+def test_merge_lse_rejects(lib):
+    f = lib.mla_merge_lse
+    assert f(FAKE, FAKE, 0, 4, 8, 512, None, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 2, 4, 8, 500, None, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(None, FAKE, 2, 4, 8, 512, None, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE + 8, FAKE, 2, 4, 8, 512, None, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(None, None, 2, 0, 8, 512, None, None, None, None) == B.MLA_OK

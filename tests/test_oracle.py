@@ -443,3 +443,46 @@ def test_sparse_ragged_list_equals_padded_list():
     b = O.mla_decode(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, None, None, w.softmax_scale,
                      sparse_slots=padded)
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+# ---------------------------------------------------------------- shard (DCP) merge
+
+@pytest.mark.parametrize("world", [1, 2, 3, 4])
+def test_round_robin_shards_merge_to_the_unsplit_decode(world):
+    w = _dense_case(50 + world, [1, 9, 40, 130], H=3, bs=16, qlens=[1, 3, 2, 1], sinks=True)
+    out, lse = _run(w)
+    lay = O.token_layout(len(w.seq_lens), w.qo_indptr)
+    T = w.num_tokens
+    outs = np.zeros((world, T, 3, 512))
+    lses = np.zeros((world, T, 3))
+    for rank in range(world):
+        K = 256
+        slots = np.full((T, K), -1, dtype=np.int64)
+        for t, (r, j, ql) in enumerate(lay):
+            pos = O.round_robin_positions(int(w.seq_lens[r]), ql, j, world, rank)
+            slots[t, :len(pos)] = O.dense_slots(w.block_table[r], w.block_size,
+                                                int(w.seq_lens[r]))[pos]
+        outs[rank], lses[rank] = O.mla_decode(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, None,
+                                              None, w.softmax_scale, sparse_slots=slots)
+    mo, ml = O.merge_lse_shards(outs, lses, sinks=w.sinks)
+    np.testing.assert_allclose(mo, out, atol=1e-12)
+    np.testing.assert_allclose(ml, lse, atol=1e-12)
+
+
+def test_shard_merge_closed_forms():
+    rng = np.random.default_rng(5)
+    o = rng.standard_normal((1, 2, 3, 512))
+    l = rng.standard_normal((1, 2, 3))
+    mo, ml = O.merge_lse_shards(o, l)        # one shard: identity
+    np.testing.assert_allclose(mo, o[0], atol=1e-14)
+    np.testing.assert_allclose(ml, l[0], atol=1e-14)
+    o2 = np.stack([o[0], o[0]])
+    l2 = np.stack([l[0], l[0]])
+    mo, ml = O.merge_lse_shards(o2, l2)      # two equal shards: same out, lse + ln 2
+    np.testing.assert_allclose(mo, o[0], atol=1e-14)
+    np.testing.assert_allclose(ml, l[0] + math.log(2), atol=1e-12)
+    l3 = np.stack([l[0], np.full_like(l[0], -np.inf)])
+    mo, ml = O.merge_lse_shards(np.stack([o[0], np.full_like(o[0], np.nan)]), l3)
+    np.testing.assert_allclose(mo, o[0], atol=1e-14)   # an empty shard is ignored
+    mo, ml = O.merge_lse_shards(np.zeros((2, 1, 1, 512)), np.full((2, 1, 1), -np.inf))
+    assert np.all(mo == 0) and np.isneginf(ml).all()
