@@ -273,6 +273,25 @@ MLA_API mla_status_t mla_merge_lse(const void* shard_out, const float* shard_lse
                                    int32_t kv_lora_rank, const float* sinks, void* out,
                                    float* lse, cudaStream_t stream);
 
+/*
+ * mla_concat_quant_q -- the q pre-step of forward_mqa ([sparse] and [dense]
+ * forward_mqa: q = ql_nope || q_pe, and for fp8 attention the static
+ * per-tensor quantisation with layer._q_scale):
+ *   out[t, h, 0:512] = ql_nope[t, h, :], out[t, h, 512:576] = q_pe[t, h, :]
+ * as bf16, or as e4m3 codes of (value / q_scale) rounded to nearest even
+ * with magnitudes above 448 saturated (the division is fp32).
+ *   ql_nope [T, H, 512] bf16, strides (elements) nope_stride_t, nope_stride_h
+ *   q_pe    [T, H, 64]  bf16, strides pe_stride_t, pe_stride_h
+ *   out     [T, H, 576] contiguous, in out_dtype
+ * The last dims are contiguous; pointers 16-byte aligned, strides multiples
+ * of 8 elements. Errors: MLA_ERR_INVALID_ARG, MLA_ERR_CUDA.
+ */
+MLA_API mla_status_t mla_concat_quant_q(const void* ql_nope, int64_t nope_stride_t,
+                                        int64_t nope_stride_h, const void* q_pe,
+                                        int64_t pe_stride_t, int64_t pe_stride_h,
+                                        int32_t num_tokens, int32_t num_heads, int32_t out_dtype,
+                                        float q_scale, void* out, cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 MLA_API const char* mla_status_string(mla_status_t status);
 

@@ -6,7 +6,7 @@ with the CUDA library and imports nothing from it.
 """
 from .mla_oracle import (  # noqa: F401
     HEAD_DIM, KV_LORA_RANK, LOG2E, LN2,
-    attend, decode_bf16, decode_e4m3fn, dense_slots, dequantize, index_convert,
+    attend, concat_quant_q, decode_bf16, decode_e4m3fn, encode_e4m3fn, dense_slots, dequantize, index_convert,
     merge_lse_shards, merge_segments, mla_decode, partition_lengths, round_robin_positions,
     segment_bounds,
     segment_partials, tile_size_for_block, token_layout, visible_len,

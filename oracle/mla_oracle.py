@@ -433,3 +433,46 @@ def round_robin_positions(seq_len: int, qlen: int, j: int, world: int, rank: int
     (``dcp_local_verify_row_lens`` counts exactly these)."""
     n = visible_len(seq_len, qlen, j)
     return np.arange(rank, n, world, dtype=np.int64)
+
+
+# ---------------------------------------------------------------------------
+# q pre-step: concat of the latent and rope parts, optional e4m3 quantisation
+# ---------------------------------------------------------------------------
+
+def _e4m3_grid():
+    codes = np.arange(0x00, 0x7F, dtype=np.uint8)          # +0 .. +448, NaN excluded
+    vals = decode_e4m3fn(codes)
+    order = np.argsort(vals, kind="stable")
+    return vals[order], codes[order]
+
+
+def encode_e4m3fn(x):
+    """Real values -> e4m3fn codes: the nearest representable value, ties to
+    the even code (mantissa LSB 0), magnitudes above 448 saturated to 448
+    (static per-tensor fp8 quantisation clamps before casting). NaN is not an
+    input here."""
+    vals, codes = _e4m3_grid()
+    a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), vals[-1])
+    hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)
+    lo = np.clip(hi - 1, 0, len(vals) - 1)
+    dlo = a - vals[lo]
+    dhi = vals[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & ((codes[hi] & 1) == 0))
+    c = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
+    neg = np.signbit(np.asarray(x, dtype=np.float64)) & (c != 0)
+    return np.where(neg, c | 0x80, c).astype(np.uint8)
+
+
+def concat_quant_q(ql_nope, q_pe, q_scale=None):
+    """``q = ql_nope || q_pe`` along the last dim (forward_mqa's concat of the
+    absorbed latent query and its rope part). With ``q_scale`` the result is
+    quantised to e4m3fn codes of ``q / q_scale``; without it the float values
+    are returned."""
+    q = np.concatenate([np.asarray(ql_nope, dtype=np.float64),
+                        np.asarray(q_pe, dtype=np.float64)], axis=-1)
+    if q_scale is None:
+        return q
+    # q / q_scale is taken in float32, the precision the kernel divides in, so
+    # both sides round the same quotient to e4m3.
+    scaled = (q.astype(np.float32) / np.float32(q_scale)).astype(np.float64)
+    return encode_e4m3fn(scaled)

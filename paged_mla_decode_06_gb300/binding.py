@@ -100,6 +100,11 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.mla_merge_lse.argtypes = [_vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, _vp, _vp, _vp, _vp]
         lib.mla_merge_lse.restype = st
+        lib.mla_concat_quant_q.argtypes = [_vp, ctypes.c_int64, ctypes.c_int64, _vp,
+                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_int32,
+                                           ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _vp,
+                                           _vp]
+        lib.mla_concat_quant_q.restype = st
         lib.mla_status_string.argtypes = [ctypes.c_int32]
         lib.mla_status_string.restype = ctypes.c_char_p
         lib.mla_last_cuda_error.argtypes = []
@@ -212,6 +217,18 @@ def mla_merge_lse(shard_out, shard_lse, *, sinks=None, out, lse, stream=None) ->
     _check("mla_merge_lse", lib.mla_merge_lse(
         _ptr(shard_out), _ptr(shard_lse), W, T, H, rank, _ptr(sinks), _ptr(out), _ptr(lse),
         _stream(stream)))
+
+
+def mla_concat_quant_q(ql_nope, q_pe, *, out, q_scale: float | None = None, stream=None) -> None:
+    """q = ql_nope || q_pe into ``out`` (bf16), or e4m3 codes of q / q_scale
+    when ``q_scale`` is given (``out`` then holds uint8 codes)."""
+    lib = load_library()
+    T, H, _ = ql_nope.shape
+    fp8 = q_scale is not None
+    _check("mla_concat_quant_q", lib.mla_concat_quant_q(
+        _ptr(ql_nope), ql_nope.stride(0), ql_nope.stride(1), _ptr(q_pe), q_pe.stride(0),
+        q_pe.stride(1), T, H, MLA_DTYPE_FP8_E4M3 if fp8 else MLA_DTYPE_BF16,
+        float(q_scale) if fp8 else 1.0, _ptr(out), _stream(stream)))
 
 
 def mla_sparse_index_convert(req_id, block_table, token_indices, *, block_size: int,

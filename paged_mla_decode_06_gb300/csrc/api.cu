@@ -392,6 +392,38 @@ mla_status_t mla_merge_lse(const void* shard_out, const float* shard_lse, int32_
   return cuda_status(mla::launch_merge_lse(m, stream));
 }
 
+mla_status_t mla_concat_quant_q(const void* ql_nope, int64_t nope_stride_t, int64_t nope_stride_h,
+                                const void* q_pe, int64_t pe_stride_t, int64_t pe_stride_h,
+                                int32_t num_tokens, int32_t num_heads, int32_t out_dtype,
+                                float q_scale, void* out, cudaStream_t stream) {
+  if (num_tokens < 0 || num_heads <= 0) return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_DTYPE_BF16 && out_dtype != MLA_DTYPE_FP8_E4M3) return MLA_ERR_INVALID_ARG;
+  if (out_dtype == MLA_DTYPE_FP8_E4M3 && !(std::isfinite(q_scale) && q_scale > 0.f))
+    return MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MLA_OK;
+  if (ql_nope == nullptr || q_pe == nullptr || out == nullptr) return MLA_ERR_INVALID_ARG;
+  if (nope_stride_h < kRank || pe_stride_h < 64 || nope_stride_t < nope_stride_h * num_heads ||
+      pe_stride_t < pe_stride_h * num_heads)
+    return MLA_ERR_INVALID_ARG;
+  // 16-byte vector loads of every 8-column group
+  if (!aligned(ql_nope, 16) || !aligned(q_pe, 16) || !aligned(out, 16) || nope_stride_t % 8 ||
+      nope_stride_h % 8 || pe_stride_t % 8 || pe_stride_h % 8)
+    return MLA_ERR_INVALID_ARG;
+  mla::QPrepParams q{};
+  q.nope = ql_nope;
+  q.nope_st = nope_stride_t;
+  q.nope_sh = nope_stride_h;
+  q.pe = q_pe;
+  q.pe_st = pe_stride_t;
+  q.pe_sh = pe_stride_h;
+  q.num_tokens = num_tokens;
+  q.num_heads = num_heads;
+  q.fp8 = out_dtype == MLA_DTYPE_FP8_E4M3 ? 1 : 0;
+  q.q_scale = q_scale;
+  q.out = out;
+  return cuda_status(mla::launch_concat_q(q, stream));
+}
+
 mla_status_t mla_sparse_index_convert(const int32_t* req_id, const int32_t* block_table,
                                       int32_t bt_rows, int32_t bt_cols, int64_t bt_row_stride,
                                       const int32_t* token_indices, int64_t ti_row_stride,

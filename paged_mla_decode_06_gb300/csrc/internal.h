@@ -69,6 +69,19 @@ struct LseMergeParams {
 };
 
 cudaError_t launch_merge_lse(const LseMergeParams& p, cudaStream_t stream);
+
+struct QPrepParams {
+  const void* nope;          // [T, H, 512] bf16, strides in elements
+  int64_t nope_st, nope_sh;
+  const void* pe;            // [T, H, 64] bf16
+  int64_t pe_st, pe_sh;
+  int32_t num_tokens, num_heads;
+  int32_t fp8;               // 1: e4m3 codes of q / q_scale; 0: bf16
+  float q_scale;
+  void* out;                 // [T, H, 576]
+};
+
+cudaError_t launch_concat_q(const QPrepParams& p, cudaStream_t stream);
 cudaError_t launch_decode_mma(int32_t kernel, bool fp8, const DecodeParams& p, dim3 grid,
                               cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);

@@ -223,3 +223,14 @@ def test_merge_lse_rejects(lib):
     assert f(None, FAKE, 2, 4, 8, 512, None, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
     assert f(FAKE + 8, FAKE, 2, 4, 8, 512, None, FAKE, FAKE, None) == B.MLA_ERR_INVALID_ARG
     assert f(None, None, 2, 0, 8, 512, None, None, None, None) == B.MLA_OK
+
+
+def test_concat_quant_q_rejects(lib):
+    f = lib.mla_concat_quant_q
+    args = [FAKE, 512 * 8, 512, FAKE, 64 * 8, 64, 4, 8]
+    assert f(*args, 7, 1.0, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(*args, 1, 0.0, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE, 512 * 8, 500, FAKE, 64 * 8, 64, 4, 8, 0, 1.0, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(FAKE + 4, 512 * 8, 512, FAKE, 64 * 8, 64, 4, 8, 0, 1.0, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(None, 512 * 8, 512, FAKE, 64 * 8, 64, 4, 8, 0, 1.0, FAKE, None) == B.MLA_ERR_INVALID_ARG
+    assert f(None, 0, 0, None, 0, 0, 0, 8, 0, 1.0, None, None) == B.MLA_OK

@@ -384,3 +384,34 @@ def test_full_sparse_sampled():
     tokens = [0, 1, 64, 127]
     ro, rl = run_oracle(w, tokens=tokens, slots=slots)
     assert_close(out[tokens], lse[tokens], ro, rl, "bf16", "full sparse")
+
+
+# ---------------------------------------------------------------- q pre-step
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_concat_quant_q_bit_exact(fp8):
+    rng = np.random.default_rng(21)
+    T, H = 9, 20
+    nope = I.float32_to_bf16_bits(rng.standard_normal((T, H, 512)).astype(np.float32) * 3)
+    pe = I.float32_to_bf16_bits(rng.standard_normal((T, H, 64)).astype(np.float32) * 3)
+    nope[0, 0, :4] = I.float32_to_bf16_bits(np.array([1e6, -1e6, 0.0, -0.0], np.float32))
+    dev = torch.device("cuda")
+    # strided views: the latent and rope parts live in one wider buffer
+    big = torch.zeros((T, H, 640), dtype=torch.int16)
+    big[..., :512] = torch.from_numpy(nope.view(np.int16))
+    big[..., 576:640] = torch.from_numpy(pe.view(np.int16))
+    big = big.to(dev).view(torch.bfloat16)
+    a, b = big[..., :512], big[..., 576:640]
+    scale = 0.0371
+    if fp8:
+        out = torch.empty((T, H, 576), dtype=torch.uint8, device=dev)
+        B.mla_concat_quant_q(a, b, out=out, q_scale=scale)
+        want = O.concat_quant_q(O.decode_bf16(nope), O.decode_bf16(pe), q_scale=scale)
+        torch.cuda.synchronize()
+        assert np.array_equal(out.cpu().numpy(), want)
+    else:
+        out = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
+        B.mla_concat_quant_q(a, b, out=out)
+        torch.cuda.synchronize()
+        want = O.concat_quant_q(O.decode_bf16(nope), O.decode_bf16(pe))
+        assert np.array_equal(out.float().cpu().numpy().astype(np.float64), want)

@@ -486,3 +486,38 @@ def test_shard_merge_closed_forms():
     np.testing.assert_allclose(mo, o[0], atol=1e-14)   # an empty shard is ignored
     mo, ml = O.merge_lse_shards(np.zeros((2, 1, 1, 512)), np.full((2, 1, 1), -np.inf))
     assert np.all(mo == 0) and np.isneginf(ml).all()
+
+
+# ---------------------------------------------------------------- q pre-step
+
+def test_e4m3_encoder_matches_torch_rounding():
+    rng = np.random.default_rng(11)
+    x = np.concatenate([rng.standard_normal(20000) * 40, rng.uniform(-448, 448, 20000),
+                        rng.standard_normal(5000) * 1e-2, [0.0, -0.0, 448.0, -448.0]])
+    x = x.astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = O.encode_e4m3fn(x)
+    same = (got == ref) | ((got & 0x7F) == 0) & ((ref & 0x7F) == 0)
+    assert same.all()
+
+
+def test_e4m3_encoder_ties_saturation_and_round_trip():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = O.decode_e4m3fn(codes)
+    back = O.encode_e4m3fn(vals)
+    assert np.array_equal(O.decode_e4m3fn(back), vals)      # every value is its own code
+    assert O.encode_e4m3fn(np.array([1000.0, -1e9]))[0] == 0x7E  # saturate to +448
+    assert O.encode_e4m3fn(np.array([-1e9]))[0] == 0xFE
+    # 1 + 1/16 lies halfway between 1 (code 0x38, even) and 1.125 (0x39): ties to even
+    assert O.encode_e4m3fn(np.array([1.0625]))[0] == 0x38
+    assert O.encode_e4m3fn(np.array([1.1875]))[0] == 0x3A   # between 1.125 (odd) and 1.25
+
+
+def test_concat_quant_q():
+    rng = np.random.default_rng(12)
+    a = rng.standard_normal((2, 3, 512))
+    b = rng.standard_normal((2, 3, 64))
+    q = O.concat_quant_q(a, b)
+    assert q.shape == (2, 3, 576) and np.array_equal(q[..., :512], a) and np.array_equal(q[..., 512:], b)
+    codes = O.concat_quant_q(a, b, q_scale=0.05)
+    np.testing.assert_allclose(O.decode_e4m3fn(codes) * 0.05, q, rtol=0.07, atol=0.05 * 2 ** -9)
