@@ -37,10 +37,19 @@ if ROOT not in sys.path:
 METRIC = ("MLA decode µs/call & KV tokens/s; HBM GB/s or MMA util as % of GB300 "
           "roofline")
 UNIT = "KV tokens/s"
-WORKLOAD = ("dsv3_bf16: DeepSeek-V3-shaped bf16 MLA decode, batch 64, 128 heads, qlen 1, "
+WORKLOADS = {
+    "dsv3": "dsv3_bf16: DeepSeek-V3-shaped bf16 MLA decode, batch {b}, 128 heads, qlen 1, "
             "seq_lens uniform in [1024, 8192], block_size 64, q/cache ~N(0,1) bf16, "
-            "scale 1/sqrt(192), random page permutation, segments chosen by the planner")
-KV_ROW_BYTES = 576 * 2          # one bf16 cache row
+            "scale 1/sqrt(192), random page permutation, segments chosen by the planner",
+    "tiny": "tiny_dense: batch 2, 16 heads, qlen 1, seq_lens {{37,130}}, block_size 16, "
+            "q/cache bf16 ~N(0,0.5^2), 4 segments, tile 16",
+    "fp8": "fp8_decode: e4m3 q+KV with per-tensor scales, batch {b}, qlen 1, 16384 KV "
+           "tokens/request, block_size 64, {h} heads",
+    "mtp": "mtp_sinks: multi-token causal decode with sinks, batch {b}, 128 heads, qlen 2-4, "
+           "seq_lens lognormal(median 4096, sigma 1) clipped to [128, 32768], bf16",
+    "sparse": "sparse_topk: 128 tokens over 16 requests, 128 heads, bf16, 65536-token cache "
+              "per request at block_size 64, top-2048 distinct indices with -1 padding",
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -53,28 +62,64 @@ def _peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def _workload(seed_offset=0, batch=64):
+def _build_workload(name, seed_offset=0, batch=None, heads=128):
     from paged_mla_decode_06_gb300 import inputs as I
-    return I.dsv3_bf16(seed=2 + seed_offset, batch=batch)
+    if name == "dsv3":
+        b = batch or 64
+        return I.dsv3_bf16(seed=2 + seed_offset, batch=b), WORKLOADS[name].format(b=b)
+    if name == "tiny":
+        return I.tiny_dense(seed=1 + seed_offset), WORKLOADS[name]
+    if name == "fp8":
+        b = batch or 52
+        return I.fp8_decode(heads, seed=3 + seed_offset, batch=b), \
+            WORKLOADS[name].format(b=b, h=heads)
+    if name == "mtp":
+        b = batch or 32
+        return I.mtp_sinks(seed=4 + seed_offset, batch=b), WORKLOADS[name].format(b=b)
+    if name == "sparse":
+        return I.sparse_topk(seed=5 + seed_offset), WORKLOADS[name]
+    raise ValueError(name)
+
+
+def _row_bytes(w):
+    return 576 * (2 if w.kv_dtype == "bf16" else 1)
+
+
+def _kv_keys(w):
+    """KV tokens attended once per request (dense) or valid slots (sparse)."""
+    import numpy as np
+    if w.sparse:
+        return int((w.topk_indices >= 0).sum())
+    return int(w.seq_lens.astype(np.int64).sum())
 
 
 def _flops(w):
-    # 2176 flop per (key, row): 1152 for q.k over 576 columns, 1024 for p.v over 512
-    return float(w.seq_lens.astype("int64").sum()) * w.num_heads * 2176.0
+    """2176 flop per (visible key, query row): 1152 for q.k over 576 columns,
+    1024 for p.v over 512 (causally masked keys are not counted)."""
+    import numpy as np
+    H = w.num_heads
+    if w.sparse:
+        return float((w.topk_indices >= 0).sum()) * H * 2176.0
+    if w.qo_indptr is None:
+        return float(w.seq_lens.astype(np.int64).sum()) * H * 2176.0
+    tot = 0
+    for r in range(w.num_reqs):
+        ql = int(w.qo_indptr[r + 1] - w.qo_indptr[r])
+        L = int(w.seq_lens[r])
+        tot += sum(max(0, L - ql + j + 1) for j in range(ql))
+    return float(tot) * H * 2176.0
 
 
 def _alg_bytes_decode(w):
-    """Algorithmic bytes of one decode launch: every KV row once, q once, the
-    block-table entries read. Segment partials are not algorithmic."""
+    """Algorithmic bytes of one decode launch: every KV row once per request
+    (or valid sparse slot), q once, the block-table entries or slot list read.
+    Segment partials are not algorithmic."""
     import numpy as np
-    keys = int(w.seq_lens.astype(np.int64).sum())
+    qb = w.num_tokens * w.num_heads * 576 * (2 if w.q_dtype == "bf16" else 1)
+    if w.sparse:
+        return _kv_keys(w) * _row_bytes(w) + qb + w.topk_indices.size * 4
     blocks = int(((w.seq_lens.astype(np.int64) + w.block_size - 1) // w.block_size).sum())
-    return keys * KV_ROW_BYTES + w.num_tokens * w.num_heads * 576 * 2 + blocks * 4 + \
-        w.num_reqs * 4
-
-
-def _alg_bytes_step(w):
-    return _alg_bytes_decode(w) + w.num_tokens * w.num_heads * (512 * 2 + 4)
+    return _kv_keys(w) * _row_bytes(w) + qb + blocks * 4 + w.num_reqs * 4
 
 
 class ClockSampler:
@@ -255,7 +300,8 @@ def run_gpu(args):
 
     BUILD.build()
     B.load_library()
-    w = _workload(seed_offset=rank, batch=args.batch)
+    w, workload = _build_workload(args.workload, seed_offset=rank, batch=args.batch,
+                                  heads=args.heads)
     kern = {"auto": B.MLA_KERNEL_AUTO, "mma": B.MLA_KERNEL_WARP_MMA,
             "tc": B.MLA_KERNEL_TCGEN05}[args.kernel]
     dw = B.DeviceWorkload(w, device=dev, kernel=kern,
@@ -297,10 +343,16 @@ def run_gpu(args):
     sm = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
     se = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
 
+    if w.sparse:
+        dw.convert()
+
     def decode_only():
-        B.mla_decode_segments(plan, dw.q, dw.cache, block_table=dw.block_table,
-                              seq_lens=dw.seq_lens, softmax_scale=w.softmax_scale,
-                              segm_output=so, segm_max=sm, segm_expsum=se)
+        B.mla_decode_segments(plan, dw.q, dw.cache,
+                              block_table=None if w.sparse else dw.block_table,
+                              seq_lens=None if w.sparse else dw.seq_lens,
+                              qo_indptr=dw.qo_indptr, sparse_slots=dw.slots,
+                              softmax_scale=w.softmax_scale, q_scale=w.q_scale,
+                              kv_scale=w.kv_scale, segm_output=so, segm_max=sm, segm_expsum=se)
 
     for _ in range(3):
         decode_only()
@@ -316,19 +368,27 @@ def run_gpu(args):
         dec_ms.append(e0.elapsed_time(e1))
     clocks = sampler.stop()
 
-    # ---- end to end through the C ABI with host buffers
-    h_q = torch.from_numpy(w.q.view(np.int16)).pin_memory()
-    h_bt = torch.from_numpy(w.block_table).pin_memory()
-    h_sl = torch.from_numpy(w.seq_lens).pin_memory()
+    # ---- end to end through the C ABI with host buffers: every step copies
+    # the step's inputs (q, block table / top-k indices, lengths) from pinned
+    # host memory and the output and LSE back; the cache is device-resident.
+    pairs = [(dw.q, torch.from_numpy(w.q.view(np.int16 if w.q_dtype == "bf16" else np.uint8)))]
+    if w.sparse:
+        pairs += [(dw.topk_indices, torch.from_numpy(w.topk_indices)),
+                  (dw.req_id, torch.from_numpy(w.req_id_per_token))]
+    else:
+        pairs += [(dw.block_table, torch.from_numpy(w.block_table)),
+                  (dw.seq_lens, torch.from_numpy(w.seq_lens))]
+        if dw.qo_indptr is not None:
+            pairs.append((dw.qo_indptr, torch.from_numpy(w.qo_indptr)))
+    pairs = [(d, h.pin_memory()) for d, h in pairs]
     h_out = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
     h_lse = torch.empty((T, H), dtype=torch.float32).pin_memory()
-    h2d = h_q.numel() * 2 + h_bt.numel() * 4 + h_sl.numel() * 4
+    h2d = sum(h.numel() * h.element_size() for _, h in pairs)
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
 
     def e2e_step():
-        dw.q.copy_(h_q, non_blocking=True)
-        dw.block_table.copy_(h_bt, non_blocking=True)
-        dw.seq_lens.copy_(h_sl, non_blocking=True)
+        for d, h in pairs:
+            d.copy_(h.view(d.dtype) if h.dtype != d.dtype else h, non_blocking=True)
         dw.forward()
         h_out.copy_(dw.out, non_blocking=True)
         h_lse.copy_(dw.lse, non_blocking=True)
@@ -347,7 +407,7 @@ def run_gpu(args):
         e1.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
 
-    keys_rank = float(w.seq_lens.astype(np.int64).sum())
+    keys_rank = float(_kv_keys(w))
     (ms, dms, ems), keys_total = aggregate_over_ranks(
         [statistics.mean(step_ms), statistics.mean(dec_ms), statistics.mean(e2e_ms)],
         keys_rank, dev if world > 1 else None)
@@ -358,8 +418,8 @@ def run_gpu(args):
         achieved = alg / (dms * 1e-3) / 1e9
         peak_bw = float(peaks["hbm_gbs"])
         tflops = _flops(w) / (dms * 1e-3) / 1e12
-        workload = WORKLOAD if args.batch == 64 else WORKLOAD.replace("batch 64",
-                                                                        f"batch {args.batch}")
+        kname = "decode_tc_kernel (tcgen05 CTA pair)" if plan.kernel == 4 else \
+            "decode_mma_kernel (warp MMA)"
         line = {
             "metric": METRIC,
             "value": keys_total / (ms * 1e-3),
@@ -372,7 +432,7 @@ def run_gpu(args):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "bf16",
+            "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3 (fp32 accumulate, bf16 out)",
             "data": "synthetic (seeded numpy; no dataset or weights)",
             "config": {"workload": workload, "num_segments": NS, "tile_size": plan.tile_size,
                        "rows_per_cta": plan.rows_per_cta, "kernel": int(plan.kernel),
@@ -381,7 +441,7 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
                          "frac": achieved / peak_bw, "traffic": None,
-                         "kernel": "decode_mma_kernel (split-K segments)",
+                         "kernel": kname,
                          "kernel_us": dms * 1e3, "algorithmic_bytes": alg,
                          "peak_source": f"hbm_gbs of {src}",
                          "tensor_tflops": tflops,
@@ -390,11 +450,11 @@ def run_gpu(args):
             "e2e": {"value": keys_total / (ems * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ems},
-            "gpu_launches": args.steps * (1 + (1 if NS > 1 else 0)),
+            "gpu_launches": args.steps * (1 + (1 if NS > 1 else 0) + (1 if w.sparse else 0)),
             "status_word": dw.status(),
             "wall_s_timed_region": wall,
         }
-        if world == 1 and not args.no_cpu_baseline:
+        if world == 1 and not args.no_cpu_baseline and args.workload == "dsv3" and not args.batch:
             line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
         else:
             line["cpu_baseline"] = None
@@ -428,7 +488,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded numpy; no dataset or weights)",
-        "config": {"workload": WORKLOAD,
+        "config": {"workload": WORKLOADS["dsv3"].format(b=64),
                    "sample": f"each step a bounded sample (~{budget:.1f} s) of the batch"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": recs[0]["cores"],
                          "kind": "oracle", "sample": recs[-1]["sample"]},
@@ -449,9 +509,12 @@ def main():
                     help="decode kernel variant (default: the planner's choice)")
     ap.add_argument("--num-segments", type=int, default=0,
                     help="split-K segments (default: the planner's choice)")
-    ap.add_argument("--batch", type=int, default=64,
-                    help="requests per batch (64 is the measured workload; smaller batches "
-                         "of the same shape are for profiler captures)")
+    ap.add_argument("--workload", default="dsv3", choices=sorted(WORKLOADS),
+                    help="dsv3 (the measured default), tiny, fp8, mtp or sparse")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests per batch (0: the workload's own; smaller batches of the "
+                         "same shape are for profiler captures)")
+    ap.add_argument("--heads", type=int, default=128, help="heads of the fp8 workload")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.impl == "reference":
