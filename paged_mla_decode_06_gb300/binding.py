@@ -286,7 +286,11 @@ class DeviceWorkload:
 
     def status(self) -> int:
         """Device status word of the workspace (0 = no kernel reported a timeout)."""
-        return int(self.workspace[:4].view(torch.int32).item()) if self.workspace is not None else 0
+        import torch
+
+        if self.workspace is None:
+            return 0
+        return int(self.workspace[:4].view(torch.int32).item())
 
     def convert(self, stream=None):
         """Top-k positions -> global slots (sparse workloads)."""

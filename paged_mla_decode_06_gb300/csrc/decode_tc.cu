@@ -554,9 +554,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
       ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kOFinal), 0, false, 35));
       fence_after_sync();
     }
-    if (ok && row_ok) {
-      const int tok = tok0 + rho / H;
-      const int head = rho % H;
+    // TMEM loads are warp-collective: every lane runs them, and only lanes
+    // with a valid row store (ok is warp-uniform).
+    if (ok) {
+      const int tok = tok0 + (row_ok ? rho / H : 0);
+      const int head = row_ok ? rho % H : 0;
       const int64_t th = static_cast<int64_t>(tok) * H + head;
       float mult;
       float lse = -INFINITY;
@@ -588,6 +590,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
 #pragma unroll
           for (int j = 0; j < 64; ++j) o[j] = 0u;
         }
+        if (!row_ok) continue;
         if (p.final_mode) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + th * kRank +
                                                 col0 + 64 * g);
@@ -608,7 +611,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
                                  __uint_as_float(o[4 * q + 2]) * mult, __uint_as_float(o[4 * q + 3]) * mult);
         }
       }
-      if (crank == 0) {
+      if (crank == 0 && row_ok) {
         if (p.final_mode) {
           p.lse[th] = lse;
         } else {
