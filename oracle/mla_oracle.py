@@ -449,8 +449,9 @@ def _e4m3_grid():
 def encode_e4m3fn(x):
     """Real values -> e4m3fn codes: the nearest representable value, ties to
     the even code (mantissa LSB 0), magnitudes above 448 saturated to 448
-    (static per-tensor fp8 quantisation clamps before casting). NaN is not an
-    input here."""
+    (static per-tensor fp8 quantisation clamps before casting), the sign kept
+    (a negative value that rounds to zero gives negative zero, 0x80). NaN is
+    not an input here."""
     vals, codes = _e4m3_grid()
     a = np.minimum(np.abs(np.asarray(x, dtype=np.float64)), vals[-1])
     hi = np.clip(np.searchsorted(vals, a, side="left"), 0, len(vals) - 1)
@@ -459,7 +460,8 @@ def encode_e4m3fn(x):
     dhi = vals[hi] - a
     pick_hi = (dhi < dlo) | ((dhi == dlo) & ((codes[hi] & 1) == 0))
     c = np.where(pick_hi, codes[hi], codes[lo]).astype(np.uint8)
-    neg = np.signbit(np.asarray(x, dtype=np.float64)) & (c != 0)
+    # the sign is kept, also for values that round to zero (negative zero 0x80)
+    neg = np.signbit(np.asarray(x, dtype=np.float64))
     return np.where(neg, c | 0x80, c).astype(np.uint8)
 
 

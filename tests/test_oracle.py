@@ -497,8 +497,7 @@ def test_e4m3_encoder_matches_torch_rounding():
     x = x.astype(np.float32)
     ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     got = O.encode_e4m3fn(x)
-    same = (got == ref) | ((got & 0x7F) == 0) & ((ref & 0x7F) == 0)
-    assert same.all()
+    assert np.array_equal(got, ref)        # signed zeros included
 
 
 def test_e4m3_encoder_ties_saturation_and_round_trip():
@@ -511,6 +510,7 @@ def test_e4m3_encoder_ties_saturation_and_round_trip():
     # 1 + 1/16 lies halfway between 1 (code 0x38, even) and 1.125 (0x39): ties to even
     assert O.encode_e4m3fn(np.array([1.0625]))[0] == 0x38
     assert O.encode_e4m3fn(np.array([1.1875]))[0] == 0x3A   # between 1.125 (odd) and 1.25
+    assert list(O.encode_e4m3fn(np.array([0.0, -0.0, -1e-6]))) == [0x00, 0x80, 0x80]
 
 
 def test_concat_quant_q():
