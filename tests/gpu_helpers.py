@@ -8,6 +8,12 @@ from paged_mla_decode_06_gb300 import binding as B
 
 TOL_OUT = {"bf16": 1e-2, "fp8": 2e-2}
 TOL_LSE = 1e-3
+# Rows that see only a handful of keys of unit-variance values lie outside
+# the specified workloads (whose outputs average hundreds of keys). There one
+# p rounded to bf16 (relative error <= 2^-9) moves the output by up to
+# 2^-9 * max|v|, and rounding the output to bf16 adds up to 2^-8 * |out|:
+# for |v|, |out| <= 4.5 that is 0.009 + 0.018 < 3e-2.
+TOL_FEW_KEYS = 3e-2
 
 
 def run_gpu(w, num_segments=None, stream=None, kernel=B.MLA_KERNEL_AUTO):
@@ -34,8 +40,8 @@ def run_oracle(w, tokens=None, slots=None):
                         qo_indptr=w.qo_indptr, sinks=w.sinks, tokens=tokens)
 
 
-def assert_close(out, lse, ref_out, ref_lse, dtype="bf16", what=""):
-    tol = TOL_OUT[dtype]
+def assert_close(out, lse, ref_out, ref_lse, dtype="bf16", what="", tol=None):
+    tol = TOL_OUT[dtype] if tol is None else tol
     assert out.shape == ref_out.shape, (out.shape, ref_out.shape)
     assert np.isfinite(out).all(), f"{what}: non-finite output"
     err = float(np.max(np.abs(out - ref_out))) if out.size else 0.0

@@ -14,7 +14,7 @@ import oracle as O
 from paged_mla_decode_06_gb300 import binding as B
 from paged_mla_decode_06_gb300 import build as BUILD
 from paged_mla_decode_06_gb300 import inputs as I
-from tests.gpu_helpers import assert_close, oracle_slots, run_gpu, run_oracle
+from tests.gpu_helpers import TOL_FEW_KEYS, assert_close, oracle_slots, run_gpu, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -186,7 +186,7 @@ def test_tcgen05_head_counts_and_short_rows(heads):
     out, lse, dw = run_gpu(w, kernel=B.MLA_KERNEL_TCGEN05)
     assert dw.plan.kernel == 4
     ref_o, ref_l = run_oracle(w)
-    assert_close(out, lse, ref_o, ref_l, "bf16", f"tcgen05 H={heads}")
+    assert_close(out, lse, ref_o, ref_l, "bf16", f"tcgen05 H={heads}", tol=TOL_FEW_KEYS)
 
 
 def test_tcgen05_segment_partials():
@@ -240,7 +240,7 @@ def test_edge_lengths(heads, bs, ns, sinks):
                       with_sinks=sinks, num_segments=ns)
     out, lse, _ = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_close(out, lse, ref_o, ref_l, "bf16", "edge lengths")
+    assert_close(out, lse, ref_o, ref_l, "bf16", "edge lengths", tol=TOL_FEW_KEYS)
     if not sinks:
         assert np.all(out[0] == 0) and np.all(np.isneginf(lse[0]))
 
@@ -252,7 +252,7 @@ def test_block_sizes(bs):
     out, lse, dw = run_gpu(w)
     assert dw.plan.tile_size == O.tile_size_for_block(bs)
     ref_o, ref_l = run_oracle(w)
-    assert_close(out, lse, ref_o, ref_l, "bf16", f"block {bs}")
+    assert_close(out, lse, ref_o, ref_l, "bf16", f"block {bs}", tol=TOL_FEW_KEYS)
 
 
 def test_multi_token_rows_and_short_sequences():
@@ -262,7 +262,7 @@ def test_multi_token_rows_and_short_sequences():
                       with_sinks=False, num_segments=2)
     out, lse, _ = run_gpu(w)
     ref_o, ref_l = run_oracle(w)
-    assert_close(out, lse, ref_o, ref_l, "bf16", "short mtp")
+    assert_close(out, lse, ref_o, ref_l, "bf16", "short mtp", tol=TOL_FEW_KEYS)
 
 
 # ---------------------------------------------------------------- sparse decode
@@ -295,7 +295,7 @@ def test_sparse_ragged_indptr(kernel):
                                 w.softmax_scale, sparse_slots=flat, sparse_indptr=cu)
     assert dw.status() == 0
     assert_close(dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), ref_o, ref_l, "bf16",
-                 "sparse ragged")
+                 "sparse ragged", tol=TOL_FEW_KEYS)
 
 
 # ---------------------------------------------------------------- invariants
