@@ -228,8 +228,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
     for (int b = 0; b < 2; ++b) {
       mbar_init(sh.bar(kSFull + b), 1);
       mbar_init(sh.bar(kPFull + b), 128);
-      mbar_init(sh.bar(kRecvFull + b), 128);
-      mbar_init(sh.bar(kPeerFree + b), 128);
+      // the receiver arms its own barrier with the 32 KB the peer sends
+      mbar_init(sh.bar(kRecvFull + b), 1);
+      // one arrival per softmax warp of the peer
+      mbar_init(sh.bar(kPeerFree + b), 4);
       mbar_init(sh.bar(kPvDone + b), 1);
     }
     mbar_init(sh.bar(kOFinal), 1);
@@ -442,12 +444,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
                         wait_phase(sh, status, sh.bar(kPeerFree + b), ((c - 2) >> 1) & 1, true, 32));
         if (!ok) break;
       }
+      // this CTA's buffer b is about to receive the peer's 32 KB for chunk c
+      if (tid == 64) mbar_arrive_expect_tx(sh.bar(kRecvFull + b), kRecvBytes);
       const uint32_t dst = recv_peer + b * kRecvBytes + r * 256;
+      const uint32_t peer_full = bar_peer + 8u * (kRecvFull + b);
 #pragma unroll
       for (int q = 0; q < 16; ++q)
-        st_cluster_v4(dst + ((q ^ (r & 15)) << 4), sr[4 * q], sr[4 * q + 1], sr[4 * q + 2],
-                      sr[4 * q + 3]);
-      mbar_arrive_cluster(bar_peer + 8u * (kRecvFull + b));
+        st_async_v4(dst + ((q ^ (r & 15)) << 4), sr[4 * q], sr[4 * q + 1], sr[4 * q + 2],
+                    sr[4 * q + 3], peer_full);
       ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kRecvFull + b), par, true, 33));
       if (!ok) break;
       const uint8_t* src = smem + C::kOffRecv + b * kRecvBytes + r * 256;
@@ -460,7 +464,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
         s[4 * q + 2] = __uint_as_float(sr[4 * q + 2]) + v.z;
         s[4 * q + 3] = __uint_as_float(sr[4 * q + 3]) + v.w;
       }
-      mbar_arrive_cluster(bar_peer + 8u * (kPeerFree + b));
+      // buffer b consumed: one release arrive per warp on the peer's barrier
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(bar_peer + 8u * (kPeerFree + b));
 
       // keys of the chunk that exist: inside the segment and, for the sparse
       // variant, with a valid slot (one ballot per 32 keys)

@@ -79,6 +79,17 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t caddr, uint32_t a, uint32
                : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory that counts its
+// bytes on that CTA's mbarrier (complete_tx): no fence is needed for the
+// receiver, which waits on its own barrier.
+__device__ __forceinline__ void st_async_v4(uint32_t caddr, uint32_t a, uint32_t b, uint32_t c,
+                                            uint32_t d, uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];\n" ::"r"(caddr),
+      "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
+      : "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int x, int y,
                                             uint32_t bar) {
