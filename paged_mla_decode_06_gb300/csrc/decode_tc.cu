@@ -73,8 +73,10 @@ struct Cfg {
   static constexpr int kOffKV = kOffQ + kQSmemBoxes * kBoxQ;
   static constexpr int kOffV16 = kOffKV + kStages * kMaxBoxes * kBoxKV;
   static constexpr int kV16Bytes = FP8 ? 4 * kBoxKV : 0;
+  // partial scores: one buffer the peer fills, one this CTA sends from
   static constexpr int kOffRecv = kOffV16 + kV16Bytes;
-  static constexpr int kOffBar = kOffRecv + 2 * kRecvBytes;
+  static constexpr int kOffSend = kOffRecv + kRecvBytes;
+  static constexpr int kOffBar = kOffSend + kRecvBytes;
   static constexpr int kSmem = kOffBar + 256 + 1024;  // barriers, TMEM slot, flag, alignment
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kStages <= 3, "barrier slots");
@@ -228,10 +230,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
     for (int b = 0; b < 2; ++b) {
       mbar_init(sh.bar(kSFull + b), 1);
       mbar_init(sh.bar(kPFull + b), 128);
-      // the receiver arms its own barrier with the 32 KB the peer sends
-      mbar_init(sh.bar(kRecvFull + b), 1);
-      // one arrival per softmax warp of the peer
-      mbar_init(sh.bar(kPeerFree + b), 4);
+      // the receiver arms its own barrier with the 32 KB the peer sends;
+      // one arrival per softmax warp of the peer frees the buffer
+      if (b == 0) {
+        mbar_init(sh.bar(kRecvFull), 1);
+        mbar_init(sh.bar(kPeerFree), 4);
+      }
       mbar_init(sh.bar(kPvDone + b), 1);
     }
     mbar_init(sh.bar(kOFinal), 1);
@@ -438,23 +442,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
       uint32_t sr[64];
       tmem_ld_32x32b_x64(tbase + lane_off + kTmemS + 64 * b, sr);
       tmem_ld_wait();
-      // exchange partial scores with the peer CTA
-      if (c >= 2) {
+      // exchange partial scores with the peer CTA: each warp stages its 32
+      // rows locally (8 KB) and one lane bulk-copies them into the peer's
+      // receive buffer, counted on the peer's barrier
+      if (lane == 0) bulk_wait_read_all();  // this warp's previous copy has left
+      __syncwarp();
+      {
+        uint8_t* snd = smem + C::kOffSend + r * 256;
+#pragma unroll
+        for (int q = 0; q < 16; ++q)
+          *reinterpret_cast<uint4*>(snd + ((q ^ (r & 15)) << 4)) =
+              make_uint4(sr[4 * q], sr[4 * q + 1], sr[4 * q + 2], sr[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c >= 1) {
         ok = __all_sync(0xffffffffu,
-                        wait_phase(sh, status, sh.bar(kPeerFree + b), ((c - 2) >> 1) & 1, true, 32));
+                        wait_phase(sh, status, sh.bar(kPeerFree), (c - 1) & 1, true, 32));
         if (!ok) break;
       }
-      // this CTA's buffer b is about to receive the peer's 32 KB for chunk c
-      if (tid == 64) mbar_arrive_expect_tx(sh.bar(kRecvFull + b), kRecvBytes);
-      const uint32_t dst = recv_peer + b * kRecvBytes + r * 256;
-      const uint32_t peer_full = bar_peer + 8u * (kRecvFull + b);
-#pragma unroll
-      for (int q = 0; q < 16; ++q)
-        st_async_v4(dst + ((q ^ (r & 15)) << 4), sr[4 * q], sr[4 * q + 1], sr[4 * q + 2],
-                    sr[4 * q + 3], peer_full);
-      ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kRecvFull + b), par, true, 33));
+      if (lane == 0)
+        bulk_copy_to_cluster(recv_peer + q4 * 8192, smem_u32(smem + C::kOffSend + q4 * 8192), 8192,
+                             bar_peer + 8u * kRecvFull);
+      if (lane == 0) bulk_commit_group();
+      if (tid == 64) mbar_arrive_expect_tx(sh.bar(kRecvFull), kRecvBytes);
+      ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kRecvFull), c & 1, true, 33));
       if (!ok) break;
-      const uint8_t* src = smem + C::kOffRecv + b * kRecvBytes + r * 256;
+      const uint8_t* src = smem + C::kOffRecv + r * 256;
       float s[64];
 #pragma unroll
       for (int q = 0; q < 16; ++q) {
@@ -464,9 +478,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
         s[4 * q + 2] = __uint_as_float(sr[4 * q + 2]) + v.z;
         s[4 * q + 3] = __uint_as_float(sr[4 * q + 3]) + v.w;
       }
-      // buffer b consumed: one release arrive per warp on the peer's barrier
+      // the receive buffer is consumed: one release arrive per warp on the
+      // peer's barrier (the peer's next bulk copy overwrites it)
+      fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(bar_peer + 8u * (kPeerFree + b));
+      if (lane == 0) mbar_arrive_cluster(bar_peer + 8u * kPeerFree);
 
       // keys of the chunk that exist: inside the segment and, for the sparse
       // variant, with a valid slot (one ballot per 32 keys)
@@ -675,6 +691,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
   }
 
   // ------------------------------------------------------------ teardown
+  if (warp >= 2 && warp < 6 && lane == 0) bulk_wait_all();  // score copies complete
   __syncwarp();
   fence_before_sync();
   __syncthreads();
