@@ -162,7 +162,8 @@ MLA_API mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan
  *                NULL for the dense variant. Mutually exclusive with qo_indptr.
  *   softmax_scale, q_scale, kv_scale: score = softmax_scale * q_scale *
  *                kv_scale * (q . k) over 576 columns; values are scaled by
- *                kv_scale. Scales are 1 for bf16.
+ *                kv_scale. All three must be finite and > 0 (1 for the
+ *                q/kv scales of bf16).
  *   sinks        [H] fp32 natural-log sink logits or NULL ([sparse]
  *                _forward_mla): a sink adds e^sink to the softmax denominator
  *                and nothing to the output.

@@ -86,7 +86,7 @@ mla_status_t check_inputs(const mla_plan_t* plan, const Inputs& in) {
   if (in.q == nullptr || in.kv == nullptr) return MLA_ERR_INVALID_ARG;
   if (!aligned(in.q, 16) || !aligned(in.kv, 16)) return MLA_ERR_INVALID_ARG;
   if (!std::isfinite(in.softmax_scale) || !std::isfinite(in.q_scale) || !std::isfinite(in.kv_scale) ||
-      !(in.q_scale > 0.f) || !(in.kv_scale > 0.f))
+      !(in.softmax_scale > 0.f) || !(in.q_scale > 0.f) || !(in.kv_scale > 0.f))
     return MLA_ERR_INVALID_ARG;
   if (p.topk > 0) {
     if (in.slots == nullptr || in.qo_indptr != nullptr) return MLA_ERR_INVALID_ARG;

@@ -495,14 +495,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
         kmask = static_cast<uint64_t>(__ballot_sync(0xffffffffu, v0)) |
                 (static_cast<uint64_t>(__ballot_sync(0xffffffffu, v1)) << 32);
       }
-      // mask and chunk maximum
+      // mask (only chunks with keys that do not exist or are causally hidden)
+      // and the chunk maximum over the raw scores (scale2 > 0), 8-way tree
       const int lim = min(seg_end, vis) - c0;
-      float mx = -INFINITY;
+      if (lim < 64 || kmask != ~0ull) {
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        s[j] = (j < lim && ((kmask >> j) & 1ull)) ? s[j] * scale2 : -INFINITY;
-        mx = fmaxf(mx, s[j]);
+        for (int j = 0; j < 64; ++j)
+          if (!(j < lim && ((kmask >> j) & 1ull))) s[j] = -INFINITY;
       }
+      float m8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+      for (int j = 8; j < 64; ++j) m8[j & 7] = fmaxf(m8[j & 7], s[j]);
+      const float mraw = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      const float mx = mraw * scale2;  // -inf stays -inf
       m_true = fmaxf(m_true, mx);
       float alpha = 1.f;
       bool resc = false;
@@ -537,18 +545,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
         }
         tmem_st_wait();
       }
-      // P = 2^(s - m_ref), into TMEM over the scores
+      // P = 2^(s * scale2 - m_ref), into TMEM over the scores; 8 partial sums
       const float base = m_ref == -INFINITY ? 0.f : m_ref;
       uint32_t pk[32];
-      float ps = 0.f;
+      float ps8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) ps8[i] = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const float p0 = fast_exp2(s[2 * j] - base);
-        const float p1 = fast_exp2(s[2 * j + 1] - base);
-        ps += p0 + p1;
+        const float p0 = fast_exp2(fmaf(s[2 * j], scale2, -base));
+        const float p1 = fast_exp2(fmaf(s[2 * j + 1], scale2, -base));
+        ps8[j & 7] += p0 + p1;
         pk[j] = pack_p<FP8>(p0, p1);
       }
-      l += ps;
+      l += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
       tmem_st_32x32b_x32(tbase + lane_off + kTmemS + 64 * b, pk);
       tmem_st_wait();
       if constexpr (!FP8) {

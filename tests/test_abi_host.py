@@ -157,6 +157,7 @@ def _fwd(lib, plan, **over):
     (dict(lse=FAKE + 2), B.MLA_ERR_INVALID_ARG),
     (dict(qs=0.0), B.MLA_ERR_INVALID_ARG),
     (dict(sc=float("nan")), B.MLA_ERR_INVALID_ARG),
+    (dict(sc=-0.07), B.MLA_ERR_INVALID_ARG),
 ])
 def test_fwd_rejects_bad_arguments(lib, over, status):
     plan = B.mla_decode_plan(_dense_problem(num_segments=1))
