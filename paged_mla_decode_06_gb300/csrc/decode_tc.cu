@@ -55,12 +55,14 @@ constexpr uint64_t kTimeoutNs = 2000000000ull;
 enum : int {
   kQFull = 0, kKvFull = 1, kKvEmpty = 4, kSFull = 7, kPFull = 9, kRecvFull = 11,
   kPeerFree = 13, kPvDone = 15, kOFinal = 17, kDrain = 18, kV16Full = 19, kQTmem = 20,
-  kNumBars = 21
+  kSRead = 21, kNumBars = 23
 };
 
 template <bool FP8, bool SPARSE = false>
 struct Cfg {
-  static constexpr int kThreads = FP8 ? 320 : 192;  // + 4 conversion warps for e4m3
+  // warp 0 loads, warp 1 issues MMAs, warps 2..5 softmax, warps 6..9 send
+  // the partial scores to the peer (and, for e4m3, widen the values to f16)
+  static constexpr int kThreads = 320;
   static constexpr int kBoxCols = FP8 ? 128 : 64;   // elements per 128-byte box row
   static constexpr int kNbox0 = FP8 ? 2 : 4;        // CTA 0: columns [0, 256)
   static constexpr int kNbox1 = FP8 ? 3 : 5;        // CTA 1: columns [256, 576 (+ zero fill))
@@ -242,6 +244,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
     mbar_init(sh.bar(kDrain), 1);
     mbar_init(sh.bar(kV16Full), 128);
     mbar_init(sh.bar(kQTmem), 128);
+    // the sender warps have read the scores of buffer b out of TMEM
+    mbar_init(sh.bar(kSRead), 128);
+    mbar_init(sh.bar(kSRead + 1), 128);
     fence_barrier_init();
   }
   if (warp == 1) {
@@ -442,29 +447,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
       uint32_t sr[64];
       tmem_ld_32x32b_x64(tbase + lane_off + kTmemS + 64 * b, sr);
       tmem_ld_wait();
-      // exchange partial scores with the peer CTA: each warp stages its 32
-      // rows locally (8 KB) and one lane bulk-copies them into the peer's
-      // receive buffer, counted on the peer's barrier
-      if (lane == 0) bulk_wait_read_all();  // this warp's previous copy has left
-      __syncwarp();
-      {
-        uint8_t* snd = smem + C::kOffSend + r * 256;
-#pragma unroll
-        for (int q = 0; q < 16; ++q)
-          *reinterpret_cast<uint4*>(snd + ((q ^ (r & 15)) << 4)) =
-              make_uint4(sr[4 * q], sr[4 * q + 1], sr[4 * q + 2], sr[4 * q + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (c >= 1) {
-        ok = __all_sync(0xffffffffu,
-                        wait_phase(sh, status, sh.bar(kPeerFree), (c - 1) & 1, true, 32));
-        if (!ok) break;
-      }
-      if (lane == 0)
-        bulk_copy_to_cluster(recv_peer + q4 * 8192, smem_u32(smem + C::kOffSend + q4 * 8192), 8192,
-                             bar_peer + 8u * kRecvFull);
-      if (lane == 0) bulk_commit_group();
+      // the peer's partial scores for this chunk (its sender warps bulk-copy
+      // them into this CTA's receive buffer)
       if (tid == 64) mbar_arrive_expect_tx(sh.bar(kRecvFull), kRecvBytes);
       ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kRecvFull), c & 1, true, 33));
       if (!ok) break;
@@ -559,6 +543,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
         pk[j] = pack_p<FP8>(p0, p1);
       }
       l += ((ps8[0] + ps8[1]) + (ps8[2] + ps8[3])) + ((ps8[4] + ps8[5]) + (ps8[6] + ps8[7]));
+      // P overwrites the scores: the sender warps must have read them
+      ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kSRead + b), par, false, 36));
+      if (!ok) break;
       tmem_st_32x32b_x32(tbase + lane_off + kTmemS + 64 * b, pk);
       tmem_st_wait();
       if constexpr (!FP8) {
@@ -653,55 +640,97 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8>::kThreads, 
         }
       }
     }
-  } else if constexpr (FP8) {
-    // ------------------------------------------------------------ e4m3 -> f16 values
+  } else {
+    // ------------------------------------------------------------ sender (+ e4m3 values)
+    // Each chunk's partial scores leave for the peer as soon as QK^T is done:
+    // the rows of this warp's TMEM quarter are staged in shared memory and
+    // one lane bulk-copies the 8 KB into the peer's receive buffer, counted
+    // on the peer's barrier. For e4m3 the same warps then widen the chunk's
+    // value columns to f16.
+    const int q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t recv_peer = map_to_rank(smem_u32(smem + C::kOffRecv), peer);
+    const uint32_t bar_peer = map_to_rank(sh.bar0, peer);
     const int ct = tid - 192;  // 0..127
     uint8_t* v16 = smem + C::kOffV16;
     bool ok = true;
     for (int c = 0; c < n_chunks && ok; ++c) {
-      const int st = c % C::kStages;
-      ok = __all_sync(0xffffffffu,
-                      wait_phase(sh, status, sh.bar(kKvFull + st), (c / C::kStages) & 1, false, 41));
+      const int b = c & 1;
+      ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kSFull + b), (c >> 1) & 1, false, 51));
       if (!ok) break;
-      if (c >= 1) {
-        // the previous chunk's P.V has finished reading the f16 values
-        ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kPvDone + ((c - 1) & 1)),
-                                                 ((c - 1) >> 1) & 1, false, 42));
+      fence_after_sync();
+      if (lane == 0) bulk_wait_read_all();  // the previous copy has left the send buffer
+      __syncwarp();
+      uint8_t* snd = smem + C::kOffSend + r * 256;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t sr[32];
+        tmem_ld_32x32b_x32(tbase + lane_off + kTmemS + 64 * b + 32 * h, sr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(snd + (((8 * h + q) ^ (r & 15)) << 4)) =
+              make_uint4(sr[4 * q], sr[4 * q + 1], sr[4 * q + 2], sr[4 * q + 3]);
+      }
+      fence_before_sync();
+      mbar_arrive(sh.bar(kSRead + b));  // the softmax may overwrite the scores with P
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (c >= 1) {  // the peer has consumed the previous chunk's scores
+        ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kPeerFree), (c - 1) & 1, true, 52));
         if (!ok) break;
       }
-      const int nvalid = min(kKeys, seg_end - (seg_start + c * kKeys));
-      const uint8_t* src = smem + C::kOffKV + (st * C::kMaxBoxes) * kBoxKV;
-      // boxes 0 and 1 of the stage hold this CTA's 256 value columns
-      for (int i = ct; i < 2 * kKeys * 8; i += 128) {
-        const int box = i >> 9;
-        const int rem = i & 511;
-        const int row = rem >> 3;
-        const int k = rem & 7;  // logical 16-byte chunk (16 e4m3 values)
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (row < nvalid)
-          v = *reinterpret_cast<const uint4*>(src + box * kBoxKV + row * 128 + ((k ^ (row & 7)) << 4));
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t h[8];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          h[2 * e] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[e] & 0xFFFF));
-          h[2 * e + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[e] >> 16));
-        }
-        const int dbox = box * 2 + (k >> 2);
-        const int lc = (k & 3) * 2;
-        uint8_t* drow = v16 + dbox * kBoxKV + row * 128;
-        *reinterpret_cast<uint4*>(drow + ((lc ^ (row & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
-        *reinterpret_cast<uint4*>(drow + (((lc + 1) ^ (row & 7)) << 4)) =
-            make_uint4(h[4], h[5], h[6], h[7]);
+      if (lane == 0) {
+        bulk_copy_to_cluster(recv_peer + q4 * 8192, smem_u32(smem + C::kOffSend + q4 * 8192), 8192,
+                             bar_peer + 8u * kRecvFull);
+        bulk_commit_group();
       }
-      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      mbar_arrive(sh.bar(kKvEmpty + st));
-      mbar_arrive(sh.bar(kV16Full));
+      if constexpr (FP8) {
+        const int st = c % C::kStages;
+        ok = __all_sync(0xffffffffu,
+                        wait_phase(sh, status, sh.bar(kKvFull + st), (c / C::kStages) & 1, false, 41));
+        if (!ok) break;
+        if (c >= 1) {
+          // the previous chunk's P.V has finished reading the f16 values
+          ok = __all_sync(0xffffffffu, wait_phase(sh, status, sh.bar(kPvDone + ((c - 1) & 1)),
+                                                   ((c - 1) >> 1) & 1, false, 42));
+          if (!ok) break;
+        }
+        const int nvalid = min(kKeys, seg_end - (seg_start + c * kKeys));
+        const uint8_t* src = smem + C::kOffKV + (st * C::kMaxBoxes) * kBoxKV;
+        // boxes 0 and 1 of the stage hold this CTA's 256 value columns
+        for (int i = ct; i < 2 * kKeys * 8; i += 128) {
+          const int box = i >> 9;
+          const int rem = i & 511;
+          const int row = rem >> 3;
+          const int k = rem & 7;  // logical 16-byte chunk (16 e4m3 values)
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (row < nvalid)
+            v = *reinterpret_cast<const uint4*>(src + box * kBoxKV + row * 128 + ((k ^ (row & 7)) << 4));
+          const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+          uint32_t hh[8];
+#pragma unroll
+          for (int e2 = 0; e2 < 4; ++e2) {
+            hh[2 * e2] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[e2] & 0xFFFF));
+            hh[2 * e2 + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[e2] >> 16));
+          }
+          const int dbox = box * 2 + (k >> 2);
+          const int lc = (k & 3) * 2;
+          uint8_t* drow = v16 + dbox * kBoxKV + row * 128;
+          *reinterpret_cast<uint4*>(drow + ((lc ^ (row & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+          *reinterpret_cast<uint4*>(drow + (((lc + 1) ^ (row & 7)) << 4)) =
+              make_uint4(hh[4], hh[5], hh[6], hh[7]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(sh.bar(kKvEmpty + st));
+        mbar_arrive(sh.bar(kV16Full));
+      }
     }
+    if (lane == 0) bulk_wait_all();  // score copies complete before teardown
   }
 
   // ------------------------------------------------------------ teardown
-  if (warp >= 2 && warp < 6 && lane == 0) bulk_wait_all();  // score copies complete
   __syncwarp();
   fence_before_sync();
   __syncthreads();
