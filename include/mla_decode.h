@@ -293,6 +293,46 @@ MLA_API mla_status_t mla_concat_quant_q(const void* ql_nope, int64_t nope_stride
                                         int32_t num_tokens, int32_t num_heads, int32_t out_dtype,
                                         float q_scale, void* out, cudaStream_t stream);
 
+/* Largest plan->workspace_bytes that mla_decode_fwd_static accepts. */
+#define MLA_STATIC_SCRATCH_BYTES ((size_t)64 << 20) /* 64 MiB */
+
+/*
+ * mla_decode_fwd_static -- mla_decode_fwd for callers that cannot allocate
+ * device memory. The pages have no counterpart: it exists for serving
+ * engines that reserve nearly all HBM for the paged KV cache at start-up and
+ * route every later allocation through their own pool, whose op interface
+ * offers no workspace argument, so a decode-time cudaMalloc would fail or is
+ * not allowed.
+ *
+ * Arguments, outputs and errors are those of mla_decode_fwd, except that the
+ * workspace is a file-scope device array of MLA_STATIC_SCRATCH_BYTES inside
+ * this library instead of a caller buffer. Nothing here calls cudaMalloc,
+ * cudaFree or an allocating library routine.
+ *   - Set-up: the first call on a device (the current one) looks up that
+ *     array's device address once and caches it; make that first call before
+ *     any stream capture begins.
+ *   - Size limit: a plan whose workspace_bytes exceeds
+ *     MLA_STATIC_SCRATCH_BYTES is rejected with MLA_ERR_WORKSPACE before any
+ *     device work. NS == 1 plans (prob.num_segments = 1) need only 256 bytes.
+ *   - Sharing: every call on a device uses the same array, which keeps the
+ *     last call's partials. Each call first clears the array's status word
+ *     (stream-ordered memset); nothing else must start at zero. Calls whose
+ *     GPU work overlaps (different streams or host threads without ordering
+ *     between them) race on the array and give undefined results; calls on
+ *     one stream are ordered and safe.
+ *   - status_out: NULL, or a device int32 that receives (stream-ordered) the
+ *     status word after the kernels: 0, or the nonzero code of a bounded
+ *     internal wait that timed out.
+ */
+MLA_API mla_status_t mla_decode_fwd_static(const mla_plan_t* plan, const void* q,
+                                           const void* kv_cache, const int32_t* block_table,
+                                           int64_t block_table_stride, const int32_t* seq_lens,
+                                           const int32_t* qo_indptr, const int32_t* sparse_slots,
+                                           const int32_t* sparse_indptr, float softmax_scale,
+                                           float q_scale, float kv_scale, const float* sinks,
+                                           void* out, float* lse, int32_t* status_out,
+                                           cudaStream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 MLA_API const char* mla_status_string(mla_status_t status);
 

@@ -86,6 +86,8 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                   ctypes.c_float, ctypes.c_float, ctypes.c_float]
         lib.mla_decode_fwd.argtypes = common + [_vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
         lib.mla_decode_fwd.restype = st
+        lib.mla_decode_fwd_static.argtypes = common + [_vp, _vp, _vp, _vp, _vp]
+        lib.mla_decode_fwd_static.restype = st
         lib.mla_decode_segments.argtypes = common + [_vp, _vp, _vp, _vp]
         lib.mla_decode_segments.restype = st
         lib.mla_merge_segments.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
@@ -186,6 +188,22 @@ def mla_decode_fwd(plan: Plan, q, kv_cache, *, block_table=None, block_table_str
         _ptr(seq_lens), _ptr(qo_indptr), _ptr(sparse_slots), _ptr(sparse_indptr),
         float(softmax_scale), float(q_scale), float(kv_scale), _ptr(sinks), _ptr(workspace),
         ws_bytes, _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def mla_decode_fwd_static(plan: Plan, q, kv_cache, *, block_table=None,
+                          block_table_stride=None, seq_lens=None, qo_indptr=None,
+                          sparse_slots=None, sparse_indptr=None, softmax_scale: float,
+                          q_scale: float = 1.0, kv_scale: float = 1.0, sinks=None, out, lse,
+                          status_out=None, stream=None) -> None:
+    """mla_decode_fwd on the library's own static device scratch (no workspace)."""
+    lib = load_library()
+    if block_table_stride is None:
+        block_table_stride = block_table.stride(0) if block_table is not None else 0
+    _check("mla_decode_fwd_static", lib.mla_decode_fwd_static(
+        ctypes.byref(plan), _ptr(q), _ptr(kv_cache), _ptr(block_table), int(block_table_stride),
+        _ptr(seq_lens), _ptr(qo_indptr), _ptr(sparse_slots), _ptr(sparse_indptr),
+        float(softmax_scale), float(q_scale), float(kv_scale), _ptr(sinks), _ptr(out), _ptr(lse),
+        _ptr(status_out), _stream(stream)))
 
 
 def mla_decode_segments(plan: Plan, q, kv_cache, *, block_table=None, block_table_stride=None,

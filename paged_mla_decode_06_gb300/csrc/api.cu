@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "internal.h"
 #include "mla_decode.h"
@@ -443,6 +444,69 @@ mla_status_t mla_sparse_index_convert(const int32_t* req_id, const int32_t* bloc
   return cuda_status(mla::launch_index_convert(req_id, block_table, bt_rows, bt_cols, bt_row_stride,
                                                token_indices, ti_row_stride, num_tokens, topk,
                                                block_size, cu_seqlens, out, stream));
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free variant: the workspace is this file-scope device array.
+// ---------------------------------------------------------------------------
+}  // extern "C"
+
+static __device__ __align__(256) unsigned char g_mla_static_scratch[MLA_STATIC_SCRATCH_BYTES];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_mla_static_scratch on the current device, looked up
+// once per device and cached.
+mla_status_t static_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kMaxDevices) return MLA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_mla_static_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (p == nullptr) return MLA_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status_t mla_decode_fwd_static(const mla_plan_t* plan, const void* q, const void* kv_cache,
+                                   const int32_t* block_table, int64_t block_table_stride,
+                                   const int32_t* seq_lens, const int32_t* qo_indptr,
+                                   const int32_t* sparse_slots, const int32_t* sparse_indptr,
+                                   float softmax_scale, float q_scale, float kv_scale,
+                                   const float* sinks, void* out, float* lse, int32_t* status_out,
+                                   cudaStream_t stream) {
+  if (plan == nullptr) return MLA_ERR_INVALID_ARG;
+  if (plan->workspace_bytes > MLA_STATIC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
+  if (plan->workspace_bytes < sizeof(int32_t) ||
+      plan->status_offset > plan->workspace_bytes - sizeof(int32_t))
+    return MLA_ERR_INVALID_ARG;
+  if (status_out != nullptr && !aligned(status_out, 4)) return MLA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  mla_status_t s = static_scratch(&scratch);
+  if (s != MLA_OK) return s;
+  uint8_t* status = static_cast<uint8_t*>(scratch) + plan->status_offset;
+  s = cuda_status(cudaMemsetAsync(status, 0, sizeof(int32_t), stream));
+  if (s != MLA_OK) return s;
+  s = mla_decode_fwd(plan, q, kv_cache, block_table, block_table_stride, seq_lens, qo_indptr,
+                     sparse_slots, sparse_indptr, softmax_scale, q_scale, kv_scale, sinks,
+                     scratch, MLA_STATIC_SCRATCH_BYTES, out, lse, stream);
+  if (s != MLA_OK || status_out == nullptr) return s;
+  return cuda_status(cudaMemcpyAsync(status_out, status, sizeof(int32_t),
+                                     cudaMemcpyDeviceToDevice, stream));
 }
 
 }  // extern "C"
