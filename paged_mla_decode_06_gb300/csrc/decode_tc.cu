@@ -19,11 +19,13 @@
 //       fp32 filling its whole TMEM; rows whose reference max moved are
 //       rescaled in TMEM before the product; the epilogue scales O by the
 //       per-row factor the score CTA sends at the end.
-// Warps: 0 TMA (q, block-table lookup, key boxes, L2 prefetch a few groups
-// ahead), 1 MMA issue, 2-5 softmax (score CTA) or O rescale + epilogue
-// (value CTA), 6-9 row gather (sparse) or e4m3 -> f16 widening of the value
-// columns (value CTA, e4m3). The value CTA re-reads the first 512 columns
-// of each row, which the score CTA has just pulled through L2.
+// Warps: 0 TMA (q, block-table lookup, key boxes), 1 MMA issue, 2-5
+// softmax (score CTA) or O rescale + epilogue (value CTA), 6-9 row gather
+// (sparse), e4m3 -> f16 widening of the value columns (value CTA, e4m3) or
+// more TMA producers (6-8): one warp issuing TMA loads moves only ~27 bytes
+// per SM clock, several keep the SM's load path busy. The value CTA re-reads
+// the first 512 columns of each row, which the score CTA has just pulled
+// through L2.
 // Every wait is bounded; on a timeout the kernel records an error code in
 // the status word, stops issuing work, drains what it issued and exits.
 #include <atomic>
@@ -55,7 +57,6 @@ constexpr uint32_t kTmemS = 0;     // score CTA: scores, 2 buffers x 128 columns
 constexpr uint32_t kTmemQ = 256;   // score CTA, bf16: q's 512 latent dims in 256 columns
 constexpr uint32_t kTmemO = 0;     // value CTA: O, 512 columns
 constexpr uint64_t kTimeoutNs = 2000000000ull;
-constexpr int kPrefetchAhead = 3;  // key groups pulled into L2 ahead of their loads
 constexpr int kMaxSlots = 16;
 
 enum : int {
@@ -80,8 +81,10 @@ static_assert(kScoreBars * 8 <= kOffTslot && kValueBars * 8 <= kOffTslot, "barri
 
 template <bool FP8, bool SPARSE>
 struct Cfg {
-  static constexpr bool kAux = FP8 || SPARSE;      // warps 6-9 have work
-  static constexpr int kThreads = kAux ? 320 : 192;
+  // warps 0 and 6-8 issue TMA loads where 6-9 have no other work
+  static constexpr int kThreads = 320;
+  static constexpr int kProdK = SPARSE ? 1 : 4;          // score CTA key-ring producers
+  static constexpr int kProdV = (FP8 || SPARSE) ? 1 : 4; // value CTA stage producers
   static constexpr int kBoxCols = FP8 ? 128 : 64;  // elements per 128-byte box row
   static constexpr int kBoxesK = FP8 ? 5 : 9;      // score CTA: 576 columns (+ zero fill)
   static constexpr int kBoxesV = FP8 ? 4 : 8;      // value CTA: 512 columns
@@ -207,34 +210,26 @@ __device__ void load_q(const Ctx& x, const TcMaps& maps) {
 
 // ------------------------------------------------------------------ score CTA: key ring (dense)
 // Box j of key group g (128 keys, two 64-row TMA boxes from their blocks)
-// goes to ring slot i % kSlots, i = g * kBoxesK + j; whole rows of the group
-// kPrefetchAhead ahead are pulled into L2 as well.
+// goes to ring slot i % kSlots, i = g * kBoxesK + j. The boxes are dealt
+// round-robin to kProdK producer warps (one issuing warp moves ~27 bytes
+// per clock; several keep the SM's load path busy).
 template <bool FP8, bool SPARSE>
-__device__ void score_ring_tma(const Ctx& x, const TcMaps& maps, const DecodeParams& p) {
+__device__ void score_ring_tma(const Ctx& x, const TcMaps& maps, const DecodeParams& p, int pidx) {
   using C = Cfg<FP8, SPARSE>;
   const int32_t* bt_row = p.block_table + static_cast<int64_t>(x.unit) * p.bt_stride;
   const int n_groups = cdiv(x.n_chunks, 2);
-  auto prefetch = [&](int g) {
-    for (int h = 0; h < 2; ++h) {
-      const int pos = x.seg_start + g * kGroup + h * kKeys;
-      if (pos >= x.seg_end) break;
-      const int row = cache_row(p, bt_row, pos);
-      for (int j = 0; j < C::kBoxesK; ++j) tma_prefetch_l2_2d(&maps.kv, C::kBoxCols * j, row);
-    }
-  };
   tma_prefetch_desc(&maps.kv);
-  for (int g = 0; g < min(n_groups, kPrefetchAhead); ++g) prefetch(g);
   // bf16: slots 0..7 hold q until the softmax warps have copied it to TMEM
   if (!FP8 && n_groups > 0 && !wait_phase(x, x.bar(kQTmem), 0, false, 10)) return;
   int i = 0;
   bool ok = true;
   for (int g = 0; g < n_groups && ok; ++g) {
-    if (g + kPrefetchAhead < n_groups) prefetch(g + kPrefetchAhead);
     const int pos0 = x.seg_start + g * kGroup;
     const int row0 = cache_row(p, bt_row, pos0);
     const bool two = pos0 + kKeys < x.seg_end;
     const int row1 = two ? cache_row(p, bt_row, pos0 + kKeys) : 0;
     for (int j = 0; j < C::kBoxesK; ++j, ++i) {
+      if (i % C::kProdK != pidx) continue;
       const int slot = i % C::kSlots;
       const int use = i / C::kSlots;
       if (use >= 1 && !wait_phase(x, x.bar(kREmpty + slot), (use - 1) & 1, false, 11)) {
@@ -247,9 +242,9 @@ __device__ void score_ring_tma(const Ctx& x, const TcMaps& maps, const DecodePar
       if (two) tma_load_2d(dst + kBox, &maps.kv, C::kBoxCols * j, row1, x.bar(kRFull + slot));
     }
   }
-  // every load issued must have landed before the CTA exits
+  // every load this warp issued must have landed before the CTA exits
   for (int k = max(0, i - C::kSlots); k < i; ++k)
-    drain_wait(x.status, x.bar(kRFull + k % C::kSlots), (k / C::kSlots) & 1, 12);
+    if (k % C::kProdK == pidx) drain_wait(x.status, x.bar(kRFull + k % C::kSlots), (k / C::kSlots) & 1, 12);
 }
 
 // ------------------------------------------------------------------ score CTA: key ring (sparse)
@@ -296,10 +291,13 @@ __device__ void score_ring_gather(const Ctx& x, const DecodeParams& p) {
 }
 
 // ------------------------------------------------------------------ value CTA: stages (dense)
+// Producer warp pidx loads the boxes j = pidx, pidx + kProdV, ... of every
+// stage; the stage's barrier completes with all kProdV arrivals and bytes.
 template <bool FP8, bool SPARSE>
-__device__ void value_stage_tma(const Ctx& x, const TcMaps& maps, const DecodeParams& p) {
+__device__ void value_stage_tma(const Ctx& x, const TcMaps& maps, const DecodeParams& p, int pidx) {
   using C = Cfg<FP8, SPARSE>;
   const int32_t* bt_row = p.block_table + static_cast<int64_t>(x.unit) * p.bt_stride;
+  const int nbox = (C::kBoxesV - pidx + C::kProdV - 1) / C::kProdV;
   tma_prefetch_desc(&maps.kv);
   int issued = 0;
   for (int c = 0; c < x.n_chunks; ++c) {
@@ -308,8 +306,8 @@ __device__ void value_stage_tma(const Ctx& x, const TcMaps& maps, const DecodePa
         !wait_phase(x, x.bar(kVEmpty + st), (c / C::kStagesV - 1) & 1, false, 16))
       break;
     const int row = cache_row(p, bt_row, x.seg_start + c * kKeys);
-    mbar_arrive_expect_tx(x.bar(kVFull + st), C::kBoxesV * kBox);
-    for (int j = 0; j < C::kBoxesV; ++j)
+    mbar_arrive_expect_tx(x.bar(kVFull + st), nbox * kBox);
+    for (int j = pidx; j < C::kBoxesV; j += C::kProdV)
       tma_load_2d(smem_u32(x.smem + C::kOffV + (st * C::kBoxesV + j) * kBox), &maps.kv,
                   C::kBoxCols * j, row, x.bar(kVFull + st));
     issued = c + 1;
@@ -875,7 +873,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
       mbar_init(x.bar(kQTmem), 128);
     } else {
       for (int s = 0; s < C::kStagesV; ++s) {
-        mbar_init(x.bar(kVFull + s), SPARSE ? 128 : 1);
+        mbar_init(x.bar(kVFull + s), SPARSE ? 128 : C::kProdV);
         // e4m3: free once widened (128 arrivals); else the P.V commit
         mbar_init(x.bar(kVEmpty + s), FP8 ? 128 : 1);
       }
@@ -905,11 +903,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
   x.tbase = *tslot;
   x.peer = map_to_rank(smem_u32(smem), crank ^ 1u);
 
+  // producer index of warps 0, 6, 7, 8 (-1: not a producer)
+  const int pidx = x.warp == 0 ? 0 : (x.warp >= 6 && x.warp <= 8 ? x.warp - 5 : -1);
   if (score) {
     if (x.warp == 0) {
       if (x.lane == 0 && x.n_chunks > 0) {
         load_q<FP8, SPARSE>(x, maps);
-        if (!SPARSE) score_ring_tma<FP8, SPARSE>(x, maps, p);
+        if (!SPARSE) score_ring_tma<FP8, SPARSE>(x, maps, p, 0);
         drain_wait(status, x.bar(kQFull), 0, 13);
       }
     } else if (x.warp == 1) {
@@ -918,18 +918,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
       score_softmax<FP8, SPARSE>(x, p);
     } else if constexpr (SPARSE) {
       score_ring_gather<SPARSE>(x, p);
+    } else {
+      if (pidx >= 1 && pidx < C::kProdK && x.lane == 0 && x.n_chunks > 0)
+        score_ring_tma<FP8, SPARSE>(x, maps, p, pidx);
     }
   } else {
-    if (x.warp == 0) {
-      if (!SPARSE && x.lane == 0) value_stage_tma<FP8, SPARSE>(x, maps, p);
-    } else if (x.warp == 1) {
+    if (x.warp == 1) {
       value_mma<FP8, SPARSE>(x);
-    } else if (x.warp < 6) {
+    } else if (x.warp >= 2 && x.warp < 6) {
       value_rows<FP8, SPARSE>(x, p);
     } else if constexpr (SPARSE) {
-      value_stage_gather<SPARSE>(x, p);
+      if (x.warp >= 6) value_stage_gather<SPARSE>(x, p);
     } else if constexpr (FP8) {
-      widen_values<SPARSE>(x);
+      if (x.warp == 0 && x.lane == 0) value_stage_tma<FP8, SPARSE>(x, maps, p, 0);
+      if (x.warp >= 6) widen_values<SPARSE>(x);
+    } else {
+      if (pidx >= 0 && pidx < C::kProdV && x.lane == 0) value_stage_tma<FP8, SPARSE>(x, maps, p, pidx);
     }
   }
 
