@@ -649,8 +649,6 @@ __device__ void value_rows(const Ctx& x, const DecodeParams& p) {
   const int r = q4 * 32 + lane;
   const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
   const int H = x.H;
-  const int rho = x.row0 + r;
-  const bool row_ok = rho < x.rows_total;
   const float* alpha_rx = reinterpret_cast<const float*>(x.smem + kOffAlpha);
   const int n = x.n_chunks;
   bool ok = true;
@@ -715,41 +713,75 @@ __device__ void value_rows(const Ctx& x, const DecodeParams& p) {
     fence_after_sync();
   }
   if (ok) ok = __all_sync(0xffffffffu, wait_phase(x, x.bar(kFinal), 0, true, 55));
-  // TMEM loads are warp-collective: every lane runs them, and only lanes
-  // with a valid row store (ok is warp-uniform).
+  // Each warp scales its 32 rows and writes them out through its quarter of
+  // the last P slot (no P arrives after the last chunk), swizzled, so that
+  // every store instruction covers four 128-byte row pieces instead of 32
+  // scattered 16-byte pieces. TMEM loads are warp-collective (ok is
+  // warp-uniform).
   if (ok) {
     const float mult = reinterpret_cast<const float*>(x.smem + kOffMult)[r];
-    const int tok = x.tok0 + (row_ok ? rho / H : 0);
-    const int head = row_ok ? rho % H : 0;
-    const int64_t th = static_cast<int64_t>(tok) * H + head;
+    uint8_t* stg = x.smem + C::kOffPRecv + ((n - 1) & 1) * kPBytes + q4 * 4096;
+    const int qc = lane & 7;  // 16-byte piece of a 128-byte row piece
+    // output bases (16-byte units) of the 8 rows this lane writes, rows
+    // 4 * it + lane / 8 of the warp's 32; null past the last valid row
+    uint4* rbase[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int rr = x.row0 + 32 * q4 + 4 * it + (lane >> 3);
+      rbase[it] = nullptr;
+      if (rr < x.rows_total) {
+        const int64_t th = static_cast<int64_t>(x.tok0 + rr / H) * H + rr % H;
+        rbase[it] = p.final_mode
+                        ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + th * kRank)
+                        : reinterpret_cast<uint4*>(p.segm_out + (th * p.num_segments + x.seg) * kRank);
+      }
+    }
+    // one 32-row x 128-byte tile: this lane's row in, four rows per store out
+    auto pass = [&](const uint32_t (&w)[32], int unit0) {
+      __syncwarp();  // the previous pass has read the staging tile
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        *reinterpret_cast<uint4*>(stg + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+            make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+      __syncwarp();
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int row = 4 * it + (lane >> 3);
+        const uint4 v = *reinterpret_cast<const uint4*>(stg + row * 128 + ((qc ^ (row & 7)) << 4));
+        if (rbase[it] != nullptr) rbase[it][unit0 + qc] = v;
+      }
+    };
 #pragma unroll 1
     for (int g = 0; g < 8; ++g) {
-      uint32_t o[64];
-      if (n > 0) {
-        tmem_ld_32x32b_x64(x.tbase + lane_off + kTmemO + 64 * g, o);
-        tmem_ld_wait();
-      } else {
+      // 16-byte units of column group g: 8 per bf16 row piece, 16 per fp32
+      const int gu = p.final_mode ? 8 * g : 16 * g;
+      if (n == 0) {  // no key: zeros, written straight out (coalesced)
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) o[j] = 0u;
-      }
-      if (!row_ok) continue;
-      if (p.final_mode) {
-        uint4* dst =
-            reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + th * kRank + 64 * g);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          dst[q] = make_uint4(
-              pack_bf16(__uint_as_float(o[8 * q + 0]) * mult, __uint_as_float(o[8 * q + 1]) * mult),
-              pack_bf16(__uint_as_float(o[8 * q + 2]) * mult, __uint_as_float(o[8 * q + 3]) * mult),
-              pack_bf16(__uint_as_float(o[8 * q + 4]) * mult, __uint_as_float(o[8 * q + 5]) * mult),
-              pack_bf16(__uint_as_float(o[8 * q + 6]) * mult, __uint_as_float(o[8 * q + 7]) * mult));
+        for (int it = 0; it < 8; ++it) {
+          if (rbase[it] == nullptr) continue;
+          rbase[it][gu + qc] = z;
+          if (!p.final_mode) rbase[it][gu + 8 + qc] = z;
         }
-      } else {
-        float4* dst = reinterpret_cast<float4*>(p.segm_out + (th * p.num_segments + x.seg) * kRank + 64 * g);
+        continue;
+      }
+      uint32_t o[64];
+      tmem_ld_32x32b_x64(x.tbase + lane_off + kTmemO + 64 * g, o);
+      tmem_ld_wait();
+      if (p.final_mode) {
+        uint32_t w[32];
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-          dst[q] = make_float4(__uint_as_float(o[4 * q]) * mult, __uint_as_float(o[4 * q + 1]) * mult,
-                               __uint_as_float(o[4 * q + 2]) * mult, __uint_as_float(o[4 * q + 3]) * mult);
+        for (int j = 0; j < 32; ++j)
+          w[j] = pack_bf16(__uint_as_float(o[2 * j]) * mult, __uint_as_float(o[2 * j + 1]) * mult);
+        pass(w, gu);
+      } else {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(__uint_as_float(o[32 * hf + j]) * mult);
+          pass(w, gu + 8 * hf);
+        }
       }
     }
   }
