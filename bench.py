@@ -110,6 +110,31 @@ def _flops(w):
     return float(tot) * H * 2176.0
 
 
+# DRAM bytes (read + write) per algorithmic byte of the tensor-core decode
+# kernel, from one ncu capture (the profile summary under profiles/ names the
+# command and the numbers), valid only for the kernel source it was taken on.
+PROFILED_TRAFFIC = {
+    "source_sha256": "f0983620a3a657f3a3088cbd1fb3b5ee9f17b3dccb51d5c68c168f52cc1ef5f0",
+    "dram_per_alg_byte": (139.019520 + 3.561728) / 138.103440,
+}
+
+
+def _profiled_traffic(alg_bytes, kernel_id):
+    """DRAM bytes of one launch scaled from the capture, or None once the
+    kernel source differs from the one profiled (or for another kernel)."""
+    import hashlib
+    if kernel_id != 4:
+        return None
+    src = os.path.join(ROOT, "paged_mla_decode_06_gb300", "csrc", "decode_tc.cu")
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    if digest != PROFILED_TRAFFIC["source_sha256"]:
+        return None
+    return alg_bytes * PROFILED_TRAFFIC["dram_per_alg_byte"]
+
+
 def _alg_bytes_decode(w):
     """Algorithmic bytes of one decode launch: every KV row once per request
     (or valid sparse slot), q once, the block-table entries or slot list read.
@@ -440,7 +465,8 @@ def run_gpu(args):
                        "l2": "flushed (256 MiB write) before every timed step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
-                         "frac": achieved / peak_bw, "traffic": None,
+                         "frac": achieved / peak_bw,
+                         "traffic": _profiled_traffic(alg, int(plan.kernel)),
                          "kernel": kname,
                          "kernel_us": dms * 1e3, "algorithmic_bytes": alg,
                          "peak_source": f"hbm_gbs of {src}",

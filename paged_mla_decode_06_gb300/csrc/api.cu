@@ -226,7 +226,26 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   const int32_t max_len = sparse ? p.topk : p.max_seq_len;
 
   int32_t ns = p.num_segments;
-  if (ns == 0) {
+  if (ns == 0 && use_tc) {
+    // One CTA pair per two SMs, one pair per (row tile, segment, unit).
+    // Estimated time in 64-key chunks: waves of pairs, each as long as the
+    // longest possible segment plus a fixed per-pair cost (~8 chunks:
+    // q load, pipeline fill, the output write) and, for NS > 1, the merge's
+    // extra pass over the partials (~1 chunk per segment).
+    const int64_t items_per_seg = static_cast<int64_t>(units > 0 ? units : 1) * row_tiles;
+    const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
+    int64_t best = -1;
+    for (int32_t cand = 1; cand <= 16; ++cand) {
+      const int64_t waves = (items_per_seg * cand + pairs - 1) / pairs;
+      const int64_t span = static_cast<int64_t>(cand) * tile;
+      const int64_t seg_keys = (max_len + span - 1) / span * tile;
+      const int64_t cost = waves * (8 + (seg_keys + 63) / 64) + (cand > 1 ? cand : 0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        ns = cand;
+      }
+    }
+  } else if (ns == 0) {
     // Enough CTAs for about two per SM, but no segment shorter than
     // ~512 keys: each extra segment costs a partial write and read.
     const int64_t per_seg = static_cast<int64_t>(units > 0 ? units : 1) * row_tiles;
