@@ -7,7 +7,7 @@
 //   score CTA (rank 0) -- S_g = Q K_g^T over all 576 columns of a 128-key
 //       group (M=128, N=128, fp32 in TMEM, two buffers; kind::f16 with q's
 //       512 latent dims resident in TMEM and its rope box in shared memory,
-//       or kind::f8f6f4 with all of q in shared memory). The keys stream
+//       or kind::f8f6f4 with all of q resident in TMEM). The keys stream
 //       through a ring of 16 KB box slots (one 128-byte column box of a
 //       group per slot), each slot released by the commit of its own MMAs.
 //       Then the masks and a base-2 online softmax with a lazily moved
@@ -54,7 +54,8 @@ constexpr int kPBytes = kRows * 128;             // P tile: 128 rows x 64 keys x
 constexpr int kMsgBytes = kPBytes + kRows * 4;   // P + one rescale factor per row
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;     // score CTA: scores, 2 buffers x 128 columns
-constexpr uint32_t kTmemQ = 256;   // score CTA, bf16: q's 512 latent dims in 256 columns
+constexpr uint32_t kTmemQ = 256;   // score CTA: q (bf16: 512 latent dims in 256 columns;
+                                   // e4m3: 640 dims, zero past 576, in 160 columns)
 constexpr uint32_t kTmemO = 0;     // value CTA: O, 512 columns
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr int kMaxSlots = 16;
@@ -92,7 +93,8 @@ struct Cfg {
   static constexpr int kUsable = 232448 - 1024;    // dynamic shared memory minus alignment slack
   // score CTA: q (bf16: the rope box; e4m3: all 5 boxes), the key ring, P staging
   static constexpr int kOffQ = kHeader;
-  static constexpr int kOffRing = kOffQ + (FP8 ? 5 : 1) * kBoxQ;
+  static constexpr int kOffRing = kOffQ + (FP8 ? 0 : 1) * kBoxQ;
+  static constexpr int kBoxesQTmem = FP8 ? 5 : 8;  // q boxes staged through ring slots into TMEM
   static constexpr int kSlots = (kUsable - kOffRing - 2 * kPBytes) / kSlot;
   static constexpr int kOffPStage = kOffRing + kSlots * kSlot;
   static constexpr int kScoreEnd = kOffPStage + 2 * kPBytes;
@@ -104,7 +106,7 @@ struct Cfg {
   static constexpr int kSmem = (kScoreEnd > kValueEnd ? kScoreEnd : kValueEnd) + 1024;
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kSlots <= kMaxSlots && kSlots >= kBoxesK, "ring slots");
-  static_assert(FP8 || kSlots >= 8, "bf16 q is staged through ring slots 0..7");
+  static_assert(kSlots >= kBoxesQTmem, "q is staged through the first ring slots");
 };
 
 struct TcMaps {
@@ -189,9 +191,10 @@ __device__ __forceinline__ int cache_row(const DecodeParams& p, const int32_t* b
 }
 
 // ------------------------------------------------------------------ score CTA: q
-// bf16: the 8 latent boxes of q land in ring slots 0..7 (copied into TMEM by
-// the softmax warps, which then free the ring), the rope box stays in
-// shared memory; e4m3: all 5 boxes stay in shared memory.
+// q's boxes land in the first ring slots (bf16: the 8 latent boxes; e4m3:
+// all 5, the last half zero-filled past column 576) and are copied into TMEM
+// by the softmax warps, which then free the ring; the bf16 rope box stays in
+// shared memory.
 template <bool FP8, bool SPARSE>
 __device__ void load_q(const Ctx& x, const TcMaps& maps) {
   using C = Cfg<FP8, SPARSE>;
@@ -200,7 +203,7 @@ __device__ void load_q(const Ctx& x, const TcMaps& maps) {
   mbar_arrive_expect_tx(x.bar(kQFull), (FP8 ? 5 : 9) * kBoxQ);
   if constexpr (FP8) {
     for (int j = 0; j < 5; ++j)
-      tma_load_2d(smem_u32(x.smem + C::kOffQ + j * kBoxQ), &maps.q, 128 * j, qrow, x.bar(kQFull));
+      tma_load_2d(smem_u32(x.smem + C::kOffRing + j * kSlot), &maps.q, 128 * j, qrow, x.bar(kQFull));
   } else {
     for (int j = 0; j < 8; ++j)
       tma_load_2d(smem_u32(x.smem + C::kOffRing + j * kSlot), &maps.q, 64 * j, qrow, x.bar(kQFull));
@@ -220,7 +223,7 @@ __device__ void score_ring_tma(const Ctx& x, const TcMaps& maps, const DecodePar
   const int n_groups = cdiv(x.n_chunks, 2);
   tma_prefetch_desc(&maps.kv);
   // bf16: slots 0..7 hold q until the softmax warps have copied it to TMEM
-  if (!FP8 && n_groups > 0 && !wait_phase(x, x.bar(kQTmem), 0, false, 10)) return;
+  if (n_groups > 0 && !wait_phase(x, x.bar(kQTmem), 0, false, 10)) return;
   int i = 0;
   bool ok = true;
   for (int g = 0; g < n_groups && ok; ++g) {
@@ -248,12 +251,21 @@ __device__ void score_ring_tma(const Ctx& x, const TcMaps& maps, const DecodePar
 }
 
 // ------------------------------------------------------------------ score CTA: key ring (sparse)
-// 128 threads, thread t = row t of the group: its 128-byte piece of each box,
-// swizzled like a TMA box; keys past the segment or with slot -1 are zeroed.
+// 128 threads copy each 128-key box, eight lanes per row (lane = 16-byte
+// piece, swizzled like a TMA box), so that every cp.async instruction moves
+// four whole 128-byte row pieces; thread t covers rows t/8 + 16k. Keys past
+// the segment or with slot -1 are zero-filled. Each thread keeps
+// kGatherDepth boxes in flight (one cp.async group per box; fewer than the
+// ring's slots, so the ring never waits on itself).
+constexpr int kGatherDepth = 7;
+
 template <bool SPARSE>
 __device__ void score_ring_gather(const Ctx& x, const DecodeParams& p) {
   using C = Cfg<false, SPARSE>;
-  const int row = x.tid - 192;
+  static_assert(kGatherDepth < C::kSlots, "gather depth below the ring size");
+  const int t = x.tid - 192;
+  const int qc = t & 7;
+  const int r0 = t >> 3;  // rows r0 + 16 k, k = 0..7
   const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
   const int n_groups = cdiv(x.n_chunks, 2);
   if (n_groups > 0 &&
@@ -262,10 +274,13 @@ __device__ void score_ring_gather(const Ctx& x, const DecodeParams& p) {
   int i = 0;
   bool ok = true;
   for (int g = 0; g < n_groups && ok; ++g) {
-    const int pos = x.seg_start + g * kGroup + row;
-    const int64_t slot_id = pos < x.seg_end ? static_cast<int64_t>(p.slots[x.list_base + pos]) : -1;
-    const uint8_t* src = slot_id >= 0 ? kvb + slot_id * (kHeadDim * 2) : kvb;
-    const uint32_t bytes = slot_id >= 0 ? 16u : 0u;
+    const uint8_t* src[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int pos = x.seg_start + g * kGroup + r0 + 16 * k;
+      const int64_t slot_id = pos < x.seg_end ? static_cast<int64_t>(p.slots[x.list_base + pos]) : -1;
+      src[k] = slot_id >= 0 ? kvb + slot_id * (kHeadDim * 2) + qc * 16 : nullptr;
+    }
     for (int j = 0; j < C::kBoxesK; ++j, ++i) {
       const int slot = i % C::kSlots;
       const int use = i / C::kSlots;
@@ -273,21 +288,24 @@ __device__ void score_ring_gather(const Ctx& x, const DecodeParams& p) {
         ok = __all_sync(0xffffffffu, wait_phase(x, x.bar(kREmpty + slot), (use - 1) & 1, false, 14));
         if (!ok) break;
       }
-      const uint32_t dst = smem_u32(x.smem + C::kOffRing + slot * kSlot + row * 128);
+      const uint32_t base = smem_u32(x.smem + C::kOffRing + slot * kSlot);
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
-        cp_async_16(dst + ((k ^ (row & 7)) << 4), src + (slot_id >= 0 ? j * 128 + k * 16 : 0), bytes);
+      for (int k = 0; k < 8; ++k) {
+        const int row = r0 + 16 * k;
+        cp_async_16(base + row * 128 + ((qc ^ (row & 7)) << 4), src[k] != nullptr ? src[k] + j * 128 : kvb,
+                    src[k] != nullptr ? 16u : 0u);
+      }
       cp_async_commit();
-      if (i >= 1) {  // the previous box's copies have landed
-        cp_async_wait<1>();
+      if (i >= kGatherDepth) {  // entry i - kGatherDepth has landed
+        cp_async_wait<kGatherDepth>();
         fence_proxy_async_smem();
-        mbar_arrive(x.bar(kRFull + (i - 1) % C::kSlots));
+        mbar_arrive(x.bar(kRFull + (i - kGatherDepth) % C::kSlots));
       }
     }
   }
   cp_async_wait<0>();
   fence_proxy_async_smem();
-  if (i >= 1) mbar_arrive(x.bar(kRFull + (i - 1) % C::kSlots));
+  for (int k = max(0, i - kGatherDepth); k < i; ++k) mbar_arrive(x.bar(kRFull + k % C::kSlots));
 }
 
 // ------------------------------------------------------------------ value CTA: stages (dense)
@@ -317,14 +335,15 @@ __device__ void value_stage_tma(const Ctx& x, const TcMaps& maps, const DecodePa
 }
 
 // ------------------------------------------------------------------ value CTA: stages (sparse)
-// 128 threads: thread t copies half of row t/2 of each chunk (16-byte pieces
-// 4h..4h+3 of every box); keys past the segment or with slot -1 are zeroed.
+// 128 threads, eight lanes per row as in the score CTA's gather: thread t
+// copies 16-byte piece t % 8 of rows t/8 + 16k (k = 0..3) of every value
+// box; keys past the segment or with slot -1 are zero-filled.
 template <bool SPARSE>
 __device__ void value_stage_gather(const Ctx& x, const DecodeParams& p) {
   using C = Cfg<false, SPARSE>;
-  const int ct = x.tid - 192;
-  const int row = ct >> 1;
-  const int half = ct & 1;
+  const int t = x.tid - 192;
+  const int qc = t & 7;
+  const int r0 = t >> 3;
   const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
   int issued = 0;
   for (int c = 0; c < x.n_chunks; ++c) {
@@ -334,30 +353,35 @@ __device__ void value_stage_gather(const Ctx& x, const DecodeParams& p) {
                                                          (c / C::kStagesV - 1) & 1, false, 18));
       if (!ok) break;
     }
-    const int pos = x.seg_start + c * kKeys + row;
-    const int64_t slot = pos < x.seg_end ? static_cast<int64_t>(p.slots[x.list_base + pos]) : -1;
-    const uint8_t* src = slot >= 0 ? kvb + slot * (kHeadDim * 2) : kvb;
-    const uint32_t bytes = slot >= 0 ? 16u : 0u;
-    const uint32_t dst = smem_u32(x.smem + C::kOffV + st * C::kBoxesV * kBox + row * 128);
+    const uint8_t* src[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int pos = x.seg_start + c * kKeys + r0 + 16 * k;
+      const int64_t slot = pos < x.seg_end ? static_cast<int64_t>(p.slots[x.list_base + pos]) : -1;
+      src[k] = slot >= 0 ? kvb + slot * (kHeadDim * 2) + qc * 16 : nullptr;
+    }
+    const uint32_t base = smem_u32(x.smem + C::kOffV + st * C::kBoxesV * kBox);
     for (int j = 0; j < C::kBoxesV; ++j) {
 #pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int k = 4 * half + kk;
-        cp_async_16(dst + j * kBox + ((k ^ (row & 7)) << 4), src + (slot >= 0 ? j * 128 + k * 16 : 0),
-                    bytes);
+      for (int k = 0; k < 4; ++k) {
+        const int row = r0 + 16 * k;
+        cp_async_16(base + j * kBox + row * 128 + ((qc ^ (row & 7)) << 4),
+                    src[k] != nullptr ? src[k] + j * 128 : kvb, src[k] != nullptr ? 16u : 0u);
       }
     }
     cp_async_commit();
-    if (c >= 1) {
-      cp_async_wait<1>();
+    // kStagesV - 1 chunks stay in flight; chunk c - (kStagesV - 1) has landed
+    if (c >= C::kStagesV - 1) {
+      cp_async_wait<C::kStagesV - 1>();
       fence_proxy_async_smem();
-      mbar_arrive(x.bar(kVFull + (c - 1) % C::kStagesV));
+      mbar_arrive(x.bar(kVFull + (c - (C::kStagesV - 1)) % C::kStagesV));
     }
     issued = c + 1;
   }
   cp_async_wait<0>();
   fence_proxy_async_smem();
-  if (issued >= 1) mbar_arrive(x.bar(kVFull + (issued - 1) % C::kStagesV));
+  for (int c = max(0, issued - (C::kStagesV - 1)); c < issued; ++c)
+    mbar_arrive(x.bar(kVFull + c % C::kStagesV));
 }
 
 // ------------------------------------------------------------------ score CTA: MMA
@@ -374,7 +398,7 @@ __device__ void score_mma(const Ctx& x) {
   const uint64_t q_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffQ), 16, 1024);
   const uint64_t ring_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffRing), 16, 1024);
   const int n_groups = cdiv(x.n_chunks, 2);
-  bool ok = n_groups == 0 || wait_phase(x, x.bar(FP8 ? kQFull : kQTmem), 0, false, 21);
+  bool ok = n_groups == 0 || wait_phase(x, x.bar(kQTmem), 0, false, 21);
   int i = 0;
   for (int g = 0; g < n_groups && ok; ++g) {
     const int b = g & 1;
@@ -392,8 +416,8 @@ __device__ void score_mma(const Ctx& x) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint32_t acc = (j | k) != 0 ? 1u : 0u;
-        if constexpr (FP8) {
-          mma_ss_f8(d, q_desc + static_cast<uint64_t>((j * kBoxQ + k * 32) >> 4), bd + 2 * k, idesc, acc);
+        if constexpr (FP8) {  // A = q in TMEM: 8 columns per 32 e4m3 dims
+          mma_ts_f8(d, x.tbase + kTmemQ + 32 * j + 8 * k, bd + 2 * k, idesc, acc);
         } else if (j < 8) {
           mma_ts(d, x.tbase + kTmemQ + 32 * j + 8 * k, bd + 2 * k, idesc, acc);
         } else {
@@ -423,13 +447,14 @@ __device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
   const int vis = !row_ok ? 0 : (SPARSE ? INT_MAX : x.part_len - x.qlen + rho / H + 1);
   const float scale2 = p.score_scale_log2;
   bool ok = true;
-  if (!FP8 && x.n_chunks > 0) {
-    // this row's 512 latent dims of q, staged by TMA in ring slots 0..7,
-    // into TMEM (packed bf16 pairs, 8 x 32 columns); then the ring is free
+  if (x.n_chunks > 0) {
+    // this row of q, staged by TMA in the first ring slots, into TMEM
+    // (bf16: the 512 latent dims as packed pairs, 8 x 32 columns; e4m3: all
+    // 576 dims packed four to a column, 5 x 32 columns); then the ring is free
     ok = __all_sync(0xffffffffu, wait_phase(x, x.bar(kQFull), 0, false, 30));
     if (ok) {
 #pragma unroll 1
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < C::kBoxesQTmem; ++j) {
         const uint8_t* src = x.smem + C::kOffRing + j * kSlot + r * 128;
         uint32_t v[32];
 #pragma unroll
