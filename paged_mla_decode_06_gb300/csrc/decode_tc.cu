@@ -84,8 +84,8 @@ template <bool FP8, bool SPARSE>
 struct Cfg {
   // warps 0 and 6-8 issue TMA loads where 6-9 have no other work
   static constexpr int kThreads = 320;
-  static constexpr int kProdK = SPARSE ? 1 : 4;          // score CTA key-ring producers
-  static constexpr int kProdV = (FP8 || SPARSE) ? 1 : 4; // value CTA stage producers
+  static constexpr int kProdK = 4;             // score CTA key-ring producer warps
+  static constexpr int kProdV = FP8 ? 1 : 4;   // value CTA stage producer warps
   static constexpr int kBoxCols = FP8 ? 128 : 64;  // elements per 128-byte box row
   static constexpr int kBoxesK = FP8 ? 5 : 9;      // score CTA: 576 columns (+ zero fill)
   static constexpr int kBoxesV = FP8 ? 4 : 8;      // value CTA: 512 columns
@@ -110,8 +110,9 @@ struct Cfg {
 };
 
 struct TcMaps {
-  CUtensorMap q;   // q viewed as [T*H rows, 576], box 128 bytes x 128 rows
-  CUtensorMap kv;  // cache viewed as [NB*BS rows, 576], box 128 bytes x 64 rows
+  CUtensorMap q;     // q viewed as [T*H rows, 576], box 128 bytes x 128 rows
+  CUtensorMap kv;    // cache viewed as [NB*BS rows, 576], box 128 bytes x 64 rows
+  CUtensorMap kv1;   // sparse: the same view, box 128 bytes x 1 row (gather4)
 };
 
 __device__ __forceinline__ void report(int* status, int code) {
@@ -251,61 +252,50 @@ __device__ void score_ring_tma(const Ctx& x, const TcMaps& maps, const DecodePar
 }
 
 // ------------------------------------------------------------------ score CTA: key ring (sparse)
-// 128 threads copy each 128-key box, eight lanes per row (lane = 16-byte
-// piece, swizzled like a TMA box), so that every cp.async instruction moves
-// four whole 128-byte row pieces; thread t covers rows t/8 + 16k. Keys past
-// the segment or with slot -1 are zero-filled. Each thread keeps
-// kGatherDepth boxes in flight (one cp.async group per box; fewer than the
-// ring's slots, so the ring never waits on itself).
-constexpr int kGatherDepth = 7;
-
+// Four gather warps. Box i = g * kBoxesK + j (128 keys of group g, columns
+// 64j..64j+63) goes to ring slot i % kSlots and is fetched by warp i % 4:
+// lane l issues one TMA gather4 of rows 4l..4l+3 (four 128-byte row pieces,
+// swizzled like a tile box), so one warp instruction moves the whole box.
+// Keys with slot -1 or past the segment read cache row 0: their scores are
+// masked by the softmax warps whatever the row holds.
 template <bool SPARSE>
-__device__ void score_ring_gather(const Ctx& x, const DecodeParams& p) {
+__device__ void score_ring_gather(const Ctx& x, const TcMaps& maps, const DecodeParams& p, int pidx) {
   using C = Cfg<false, SPARSE>;
-  static_assert(kGatherDepth < C::kSlots, "gather depth below the ring size");
-  const int t = x.tid - 192;
-  const int qc = t & 7;
-  const int r0 = t >> 3;  // rows r0 + 16 k, k = 0..7
-  const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
+  const int lane = x.lane;
   const int n_groups = cdiv(x.n_chunks, 2);
+  tma_prefetch_desc(&maps.kv1);
   if (n_groups > 0 &&
       !__all_sync(0xffffffffu, wait_phase(x, x.bar(kQTmem), 0, false, 15)))
     return;
   int i = 0;
   bool ok = true;
   for (int g = 0; g < n_groups && ok; ++g) {
-    const uint8_t* src[8];
+    int r[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int pos = x.seg_start + g * kGroup + r0 + 16 * k;
-      const int64_t slot_id = pos < x.seg_end ? static_cast<int64_t>(p.slots[x.list_base + pos]) : -1;
-      src[k] = slot_id >= 0 ? kvb + slot_id * (kHeadDim * 2) + qc * 16 : nullptr;
+    for (int k = 0; k < 4; ++k) {
+      const int pos = x.seg_start + g * kGroup + 4 * lane + k;
+      const int slot_id = pos < x.seg_end ? p.slots[x.list_base + pos] : -1;
+      r[k] = slot_id >= 0 ? slot_id : 0;
     }
     for (int j = 0; j < C::kBoxesK; ++j, ++i) {
+      if (i % C::kProdK != pidx) continue;
       const int slot = i % C::kSlots;
       const int use = i / C::kSlots;
       if (use >= 1) {
         ok = __all_sync(0xffffffffu, wait_phase(x, x.bar(kREmpty + slot), (use - 1) & 1, false, 14));
         if (!ok) break;
       }
-      const uint32_t base = smem_u32(x.smem + C::kOffRing + slot * kSlot);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int row = r0 + 16 * k;
-        cp_async_16(base + row * 128 + ((qc ^ (row & 7)) << 4), src[k] != nullptr ? src[k] + j * 128 : kvb,
-                    src[k] != nullptr ? 16u : 0u);
-      }
-      cp_async_commit();
-      if (i >= kGatherDepth) {  // entry i - kGatherDepth has landed
-        cp_async_wait<kGatherDepth>();
-        fence_proxy_async_smem();
-        mbar_arrive(x.bar(kRFull + (i - kGatherDepth) % C::kSlots));
-      }
+      if (lane == 0) mbar_arrive_expect_tx(x.bar(kRFull + slot), kSlot);
+      __syncwarp();
+      tma_gather4(smem_u32(x.smem + C::kOffRing + slot * kSlot + 512 * lane), &maps.kv1, 64 * j, r[0], r[1],
+                  r[2], r[3], x.bar(kRFull + slot));
     }
   }
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
-  for (int k = max(0, i - kGatherDepth); k < i; ++k) mbar_arrive(x.bar(kRFull + k % C::kSlots));
+  // every gather this warp issued must have landed before the CTA exits
+  if (lane == 0)
+    for (int k = max(0, i - C::kSlots); k < i; ++k)
+      if (k % C::kProdK == pidx) drain_wait(x.status, x.bar(kRFull + k % C::kSlots), (k / C::kSlots) & 1, 12);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ value CTA: stages (dense)
@@ -335,16 +325,18 @@ __device__ void value_stage_tma(const Ctx& x, const TcMaps& maps, const DecodePa
 }
 
 // ------------------------------------------------------------------ value CTA: stages (sparse)
-// 128 threads, eight lanes per row as in the score CTA's gather: thread t
-// copies 16-byte piece t % 8 of rows t/8 + 16k (k = 0..3) of every value
-// box; keys past the segment or with slot -1 are zero-filled.
+// Four gather warps; warp w fetches value boxes w and w + 4 of each 64-key
+// chunk: lane l issues one TMA gather4 of rows 4(l % 16)..4(l % 16) + 3 of
+// box w + 4 (l / 16). A key with slot -1 or past the segment reads the row of
+// the chunk's first valid key (its P is zero, and that row is finite wherever
+// the exact result is); a chunk without a valid key is zero-filled by stores.
 template <bool SPARSE>
-__device__ void value_stage_gather(const Ctx& x, const DecodeParams& p) {
+__device__ void value_stage_gather(const Ctx& x, const TcMaps& maps, const DecodeParams& p, int pidx) {
   using C = Cfg<false, SPARSE>;
-  const int t = x.tid - 192;
-  const int qc = t & 7;
-  const int r0 = t >> 3;
-  const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
+  static_assert(C::kBoxesV == 2 * C::kProdV, "two value boxes per gather warp");
+  const int lane = x.lane;
+  const int jbox = pidx + C::kProdV * (lane >> 4);
+  tma_prefetch_desc(&maps.kv1);
   int issued = 0;
   for (int c = 0; c < x.n_chunks; ++c) {
     const int st = c % C::kStagesV;
@@ -353,35 +345,39 @@ __device__ void value_stage_gather(const Ctx& x, const DecodeParams& p) {
                                                          (c / C::kStagesV - 1) & 1, false, 18));
       if (!ok) break;
     }
-    const uint8_t* src[4];
+    int r[4];
+    int first = -1;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const int pos = x.seg_start + c * kKeys + r0 + 16 * k;
-      const int64_t slot = pos < x.seg_end ? static_cast<int64_t>(p.slots[x.list_base + pos]) : -1;
-      src[k] = slot >= 0 ? kvb + slot * (kHeadDim * 2) + qc * 16 : nullptr;
+      const int pos = x.seg_start + c * kKeys + 4 * (lane & 15) + k;
+      r[k] = pos < x.seg_end ? p.slots[x.list_base + pos] : -1;
+      if (first < 0 && r[k] >= 0) first = r[k];
     }
-    const uint32_t base = smem_u32(x.smem + C::kOffV + st * C::kBoxesV * kBox);
-    for (int j = 0; j < C::kBoxesV; ++j) {
+    const uint32_t have = __ballot_sync(0xffffffffu, first >= 0) & 0xffffu;
+    uint8_t* stage = x.smem + C::kOffV + st * C::kBoxesV * kBox;
+    if (have != 0) {
+      const int sub = __shfl_sync(0xffffffffu, first, __ffs(have) - 1);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int row = r0 + 16 * k;
-        cp_async_16(base + j * kBox + row * 128 + ((qc ^ (row & 7)) << 4),
-                    src[k] != nullptr ? src[k] + j * 128 : kvb, src[k] != nullptr ? 16u : 0u);
-      }
-    }
-    cp_async_commit();
-    // kStagesV - 1 chunks stay in flight; chunk c - (kStagesV - 1) has landed
-    if (c >= C::kStagesV - 1) {
-      cp_async_wait<C::kStagesV - 1>();
+      for (int k = 0; k < 4; ++k) r[k] = r[k] >= 0 ? r[k] : sub;
+      if (lane == 0) mbar_arrive_expect_tx(x.bar(kVFull + st), 2 * kBox);
+      __syncwarp();
+      tma_gather4(smem_u32(stage + jbox * kBox + 512 * (lane & 15)), &maps.kv1, 64 * jbox, r[0], r[1], r[2],
+                  r[3], x.bar(kVFull + st));
+    } else {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int b = 0; b < 2; ++b)
+        for (int q = lane; q < kBox / 16; q += 32)
+          reinterpret_cast<uint4*>(stage + (pidx + C::kProdV * b) * kBox)[q] = z;
       fence_proxy_async_smem();
-      mbar_arrive(x.bar(kVFull + (c - (C::kStagesV - 1)) % C::kStagesV));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(x.bar(kVFull + st));
     }
     issued = c + 1;
   }
-  cp_async_wait<0>();
-  fence_proxy_async_smem();
-  for (int c = max(0, issued - (C::kStagesV - 1)); c < issued; ++c)
-    mbar_arrive(x.bar(kVFull + c % C::kStagesV));
+  if (lane == 0)
+    for (int c = max(0, issued - C::kStagesV); c < issued; ++c)
+      drain_wait(x.status, x.bar(kVFull + c % C::kStagesV), (c / C::kStagesV) & 1, 17);
+  __syncwarp();
 }
 
 // ------------------------------------------------------------------ score CTA: MMA
@@ -917,8 +913,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
     *x.abort = 0;
     if (score) {
       for (int s = 0; s < C::kSlots; ++s) {
-        // sparse: every gather thread arrives after its copies land
-        mbar_init(x.bar(kRFull + s), SPARSE ? 128 : 1);
+        mbar_init(x.bar(kRFull + s), 1);
         mbar_init(x.bar(kREmpty + s), 1);
       }
       for (int b = 0; b < 2; ++b) {
@@ -930,7 +925,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
       mbar_init(x.bar(kQTmem), 128);
     } else {
       for (int s = 0; s < C::kStagesV; ++s) {
-        mbar_init(x.bar(kVFull + s), SPARSE ? 128 : C::kProdV);
+        mbar_init(x.bar(kVFull + s), C::kProdV);
         // e4m3: free once widened (128 arrivals); else the P.V commit
         mbar_init(x.bar(kVEmpty + s), FP8 ? 128 : 1);
       }
@@ -974,7 +969,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
     } else if (x.warp < 6) {
       score_softmax<FP8, SPARSE>(x, p);
     } else if constexpr (SPARSE) {
-      score_ring_gather<SPARSE>(x, p);
+      if (x.warp >= 6 && x.n_chunks > 0) score_ring_gather<SPARSE>(x, maps, p, x.warp - 6);
     } else {
       if (pidx >= 1 && pidx < C::kProdK && x.lane == 0 && x.n_chunks > 0)
         score_ring_tma<FP8, SPARSE>(x, maps, p, pidx);
@@ -985,7 +980,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
     } else if (x.warp >= 2 && x.warp < 6) {
       value_rows<FP8, SPARSE>(x, p);
     } else if constexpr (SPARSE) {
-      if (x.warp >= 6) value_stage_gather<SPARSE>(x, p);
+      if (x.warp >= 6) value_stage_gather<SPARSE>(x, maps, p, x.warp - 6);
     } else if constexpr (FP8) {
       if (x.warp == 0 && x.lane == 0) value_stage_tma<FP8, SPARSE>(x, maps, p, 0);
       if (x.warp >= 6) widen_values<SPARSE>(x);
@@ -1061,13 +1056,15 @@ int decode_tc_smem_bytes(bool fp8) {
 
 cudaError_t launch_decode_tc(const DecodeParams& p, bool fp8, int64_t q_rows, int64_t kv_rows,
                              dim3 grid, int* status, cudaStream_t stream) {
-  TcMaps maps;
+  TcMaps maps{};
   cudaError_t e = make_map(&maps.q, p.q, static_cast<uint64_t>(q_rows), kRows, fp8);
   if (e != cudaSuccess) return e;
   e = make_map(&maps.kv, p.kv, static_cast<uint64_t>(kv_rows), kKeys, fp8);
   if (e != cudaSuccess) return e;
   if (p.slots != nullptr) {
     if (fp8) return cudaErrorNotSupported;
+    e = make_map(&maps.kv1, p.kv, static_cast<uint64_t>(kv_rows), 1, false);
+    if (e != cudaSuccess) return e;
     return launch_variant<false, true>(maps, p, grid, status, stream);
   }
   return fp8 ? launch_variant<true, false>(maps, p, grid, status, stream)

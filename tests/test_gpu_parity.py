@@ -279,6 +279,44 @@ def test_sparse_small(ns, kernel):
 
 
 @pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
+@pytest.mark.parametrize("ns", [1, 3])
+def test_sparse_invalid_chunks_nan_rows(ns, kernel):
+    """Slot lists with whole 64-key chunks of -1, a token with a single valid
+    slot, one with none, and every cache row that no valid slot names set to
+    NaN: unused rows must not reach the output (softmax weight 0 times NaN)."""
+    w = I.sparse_topk(num_reqs=2, tokens_per_req=2, cache_tokens=2048, topk=256, max_pad=0)
+    slots = oracle_slots(w).astype(np.int32)
+    slots[0, 64:128] = -1             # one aligned chunk without a valid key
+    slots[0, 200:] = -1               # a ragged tail of -1
+    keep = slots[1, 137]
+    slots[1, :] = -1
+    slots[1, 137] = keep              # a single valid key
+    slots[2, :] = -1                  # none at all
+    slots[3, 1:64:2] = -1             # every other key of the first chunk
+    valid = np.unique(slots[slots >= 0])
+    flat_cache = w.cache.reshape(-1, w.cache.shape[-1])
+    poison = np.ones(flat_cache.shape[0], dtype=bool)
+    poison[valid] = False
+    flat_cache[poison] = 0x7FC0       # bf16 quiet NaN
+    lens = np.full(4, 256)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    flat = slots.reshape(-1).copy()
+    dw = B.DeviceWorkload(w, num_segments=ns, kernel=kernel)
+    dev = dw.device
+    B.mla_decode_fwd(dw.plan, dw.q, dw.cache, sparse_slots=torch.from_numpy(flat).to(dev),
+                     sparse_indptr=torch.from_numpy(cu).to(dev), softmax_scale=w.softmax_scale,
+                     workspace=dw.workspace, out=dw.out, lse=dw.lse)
+    torch.cuda.synchronize()
+    ref_o, ref_l = O.mla_decode(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, None, None,
+                                w.softmax_scale, sparse_slots=flat, sparse_indptr=cu)
+    assert dw.status() == 0
+    out = dw.out.float().cpu().numpy()
+    assert not np.isnan(out).any()
+    assert_close(out, dw.lse.cpu().numpy(), ref_o, ref_l, "bf16", "sparse invalid chunks",
+                 tol=TOL_FEW_KEYS)
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=KIDS)
 def test_sparse_ragged_indptr(kernel):
     w = I.sparse_topk(num_reqs=2, tokens_per_req=3, cache_tokens=2048, topk=256, max_pad=0)
     slots = oracle_slots(w)
