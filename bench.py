@@ -371,7 +371,21 @@ def run_gpu(args):
     if w.sparse:
         dw.convert()
 
+    balanced = plan.schedule == 1
+    if balanced:  # the work list the step computed, for the same lengths
+        B.mla_decode_schedule(plan, seq_lens=None if w.sparse else dw.seq_lens,
+                              qo_indptr=dw.qo_indptr, workspace=dw.workspace)
+
     def decode_only():
+        if balanced:  # the decode kernel of the step: same launch, same work list
+            B.mla_decode_items(plan, dw.q, dw.cache,
+                               block_table=None if w.sparse else dw.block_table,
+                               seq_lens=None if w.sparse else dw.seq_lens,
+                               qo_indptr=dw.qo_indptr, sparse_slots=dw.slots,
+                               softmax_scale=w.softmax_scale, q_scale=w.q_scale,
+                               kv_scale=w.kv_scale, sinks=dw.sinks, workspace=dw.workspace,
+                               out=dw.out, lse=dw.lse)
+            return
         B.mla_decode_segments(plan, dw.q, dw.cache,
                               block_table=None if w.sparse else dw.block_table,
                               seq_lens=None if w.sparse else dw.seq_lens,
@@ -460,6 +474,7 @@ def run_gpu(args):
             "dtype": "bf16" if w.kv_dtype == "bf16" else "e4m3 (fp32 accumulate, bf16 out)",
             "data": "synthetic (seeded numpy; no dataset or weights)",
             "config": {"workload": workload, "num_segments": NS, "tile_size": plan.tile_size,
+                       "schedule": "balanced" if balanced else "uniform",
                        "rows_per_cta": plan.rows_per_cta, "kernel": int(plan.kernel),
                        "kv_tokens_per_gpu": int(keys_rank),
                        "l2": "flushed (256 MiB write) before every timed step",
@@ -476,7 +491,8 @@ def run_gpu(args):
             "e2e": {"value": keys_total / (ems * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": ems},
-            "gpu_launches": args.steps * (1 + (1 if NS > 1 else 0) + (1 if w.sparse else 0)),
+            "gpu_launches": args.steps * ((3 if balanced else 1 + (1 if NS > 1 else 0)) +
+                                          (1 if w.sparse else 0)),
             "status_word": dw.status(),
             "wall_s_timed_region": wall,
         }

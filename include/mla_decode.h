@@ -120,7 +120,11 @@ typedef struct {
   int32_t row_tiles;           /* row tiles per request (dense) or token (sparse) */
   int32_t grid_x, grid_y, grid_z;
   int32_t num_sms;
-  int32_t reserved[4];
+  int32_t schedule;            /* 1: balanced schedule (see mla_decode_plan), else 0 */
+  int32_t max_items;           /* balanced: work items the decode grid holds */
+  int32_t split_items;         /* balanced: partial slots of 128 rows, two per
+                                  CTA pair (2 * (num_sms / 2)) */
+  int32_t reserved;
   size_t workspace_bytes;      /* bytes mla_decode_fwd needs (>= 256) */
   size_t status_offset;        /* workspace layout, 256-B aligned pieces: a device */
   size_t segm_output_offset;   /* status word (int32) at offset 0, then, when */
@@ -135,6 +139,23 @@ typedef struct {
  * tile_size = min(128, largest power of two dividing block_size)
  * ([dense] _segmented_mla_page_size); the sparse variant has no page
  * structure and uses a 64-entry tile.
+ * Balanced schedule: when the tensor-core kernel runs and prob->num_segments
+ * is 0, the plan sets schedule = 1 and num_segments = 1, and mla_decode_fwd
+ * sizes the segments on the device from the lengths of the call (the work
+ * list of [sparse] _forward_mla's persistent path, work_indptr /
+ * reduce_indptr / reduce_partial_map). Rows (a unit, i.e. a dense request or
+ * a sparse token, times its 128-query-row tiles) of g = cdiv(len, 128) key
+ * groups are laid end to end and the sequence of all groups is cut every
+ * W = cdiv(total, num_sms / 2) groups, cuts within W / 8 of a row's ends
+ * dropped; the pieces run longest first (max_items = rows + num_sms / 2).
+ * Unsplit rows are written by the decode kernel itself; split rows write
+ * base-2 partials to 128-row slots of the workspace (split_items =
+ * 2 * (num_sms / 2) of them) and mla_merge_items combines them. Workspace
+ * layout: status block, item count at 256, items (32 bytes each, max_items
+ * of them) at 512, the unit table (int32 pairs {first slot or -1, pieces}
+ * per unit and row tile) at the next 256-byte boundary, then segm_output
+ * [split_items * 128, 512], segm_max and segm_expsum [split_items * 128] at
+ * the plan's offsets.
  * Errors: MLA_ERR_INVALID_ARG for NULL pointers or inconsistent sizes,
  * MLA_ERR_UNSUPPORTED for head_dim != 576, kv_lora_rank != 512,
  * num_heads > 128, q_dtype != kv_dtype, or topk not a multiple of 128.
@@ -144,6 +165,8 @@ MLA_API mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan
 /*
  * mla_decode_fwd -- the whole decode: split-K segments, then the merge
  * (skipped when NS == 1: the segment kernel then writes out and lse itself).
+ * Under a balanced plan: mla_decode_schedule, mla_decode_items and
+ * mla_merge_items in turn.
  *
  *   q            [T, H, 576] in q_dtype ([dense] forward_mqa: ql_nope || q_pe)
  *   kv_cache     [num_blocks, block_size, 576] in kv_dtype
@@ -185,6 +208,46 @@ MLA_API mla_status_t mla_decode_fwd(const mla_plan_t* plan, const void* q, const
                             float softmax_scale, float q_scale, float kv_scale,
                             const float* sinks, void* workspace, size_t workspace_bytes,
                             void* out, float* lse, cudaStream_t stream);
+
+/*
+ * The three stages of mla_decode_fwd under a balanced plan (schedule == 1),
+ * for callers that compute the work list once per step (it depends only on
+ * the lengths) or time the stages apart. Each returns MLA_ERR_INVALID_ARG for a plan without the
+ * balanced schedule and MLA_ERR_WORKSPACE for a missing or short workspace.
+ *
+ * mla_decode_schedule -- the work list of the plan's balanced schedule into
+ *   the workspace, from seq_lens / qo_indptr (dense) or sparse_indptr
+ *   (sparse; NULL means topk entries per token). One block on `stream`.
+ */
+MLA_API mla_status_t mla_decode_schedule(const mla_plan_t* plan, const int32_t* seq_lens,
+                                         const int32_t* qo_indptr, const int32_t* sparse_indptr,
+                                         void* workspace, size_t workspace_bytes,
+                                         cudaStream_t stream);
+
+/*
+ * mla_decode_items -- the decode kernel over the work list in the
+ *   workspace, written by mla_decode_schedule for the same lengths (one list
+ *   serves any number of calls): out and lse of unsplit rows, base-2
+ *   partials of split rows in the workspace's slots. Arguments as
+ *   mla_decode_fwd.
+ */
+MLA_API mla_status_t mla_decode_items(const mla_plan_t* plan, const void* q, const void* kv_cache,
+                                      const int32_t* block_table, int64_t block_table_stride,
+                                      const int32_t* seq_lens, const int32_t* qo_indptr,
+                                      const int32_t* sparse_slots, const int32_t* sparse_indptr,
+                                      float softmax_scale, float q_scale, float kv_scale,
+                                      const float* sinks, void* workspace, size_t workspace_bytes,
+                                      void* out, float* lse, cudaStream_t stream);
+
+/*
+ * mla_merge_items -- out and lse of the split rows from their partial slots
+ *   ([merge] merge_mla_segments_triton weights, sinks folded as there);
+ *   rows of unsplit units are left untouched. qo_indptr as given to the
+ *   decode (dense multi-token requests), else NULL.
+ */
+MLA_API mla_status_t mla_merge_items(const mla_plan_t* plan, const int32_t* qo_indptr,
+                                     const float* sinks, void* workspace, size_t workspace_bytes,
+                                     void* out, float* lse, cudaStream_t stream);
 
 /*
  * mla_decode_segments -- the split-K stage alone: base-2 partials of every

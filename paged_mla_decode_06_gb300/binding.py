@@ -50,12 +50,10 @@ class Problem(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [("prob", Problem)] + [(n, ctypes.c_int32) for n in (
         "num_segments", "tile_size", "kernel", "rows_per_cta", "row_tiles", "grid_x", "grid_y",
-        "grid_z", "num_sms")] + [("reserved", ctypes.c_int32 * 4),
-                                 ("workspace_bytes", ctypes.c_size_t),
-                                 ("status_offset", ctypes.c_size_t),
-                                 ("segm_output_offset", ctypes.c_size_t),
-                                 ("segm_max_offset", ctypes.c_size_t),
-                                 ("segm_expsum_offset", ctypes.c_size_t)]
+        "grid_z", "num_sms", "schedule", "max_items", "split_items", "reserved")] + [
+        ("workspace_bytes", ctypes.c_size_t), ("status_offset", ctypes.c_size_t),
+        ("segm_output_offset", ctypes.c_size_t), ("segm_max_offset", ctypes.c_size_t),
+        ("segm_expsum_offset", ctypes.c_size_t)]
 
 
 _lib = None
@@ -90,6 +88,15 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
         lib.mla_decode_fwd_static.restype = st
         lib.mla_decode_segments.argtypes = common + [_vp, _vp, _vp, _vp]
         lib.mla_decode_segments.restype = st
+        lib.mla_decode_schedule.argtypes = [ctypes.POINTER(Plan), _vp, _vp, _vp, _vp,
+                                            ctypes.c_size_t, _vp]
+        lib.mla_decode_schedule.restype = st
+        lib.mla_decode_items.argtypes = common + [_vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
+        lib.mla_decode_items.restype = st
+        lib.mla_merge_items.argtypes = [ctypes.POINTER(Plan), _vp, _vp, _vp, ctypes.c_size_t,
+                                        _vp, _vp, _vp]
+        lib.mla_merge_items.restype = st
+
         lib.mla_merge_segments.argtypes = [_vp, _vp, _vp, _vp, ctypes.c_int32, ctypes.c_int32,
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _vp,
                                            ctypes.c_int32, _vp, _vp, _vp]
@@ -204,6 +211,43 @@ def mla_decode_fwd_static(plan: Plan, q, kv_cache, *, block_table=None,
         _ptr(seq_lens), _ptr(qo_indptr), _ptr(sparse_slots), _ptr(sparse_indptr),
         float(softmax_scale), float(q_scale), float(kv_scale), _ptr(sinks), _ptr(out), _ptr(lse),
         _ptr(status_out), _stream(stream)))
+
+
+def _ws_bytes(workspace) -> int:
+    return 0 if workspace is None else workspace.numel() * workspace.element_size()
+
+
+def mla_decode_schedule(plan: Plan, *, seq_lens=None, qo_indptr=None, sparse_indptr=None,
+                        workspace, stream=None) -> None:
+    """Balanced plans: the work list into ``workspace``."""
+    lib = load_library()
+    _check("mla_decode_schedule", lib.mla_decode_schedule(
+        ctypes.byref(plan), _ptr(seq_lens), _ptr(qo_indptr), _ptr(sparse_indptr),
+        _ptr(workspace), _ws_bytes(workspace), _stream(stream)))
+
+
+def mla_decode_items(plan: Plan, q, kv_cache, *, block_table=None, block_table_stride=None,
+                     seq_lens=None, qo_indptr=None, sparse_slots=None, sparse_indptr=None,
+                     softmax_scale: float, q_scale: float = 1.0, kv_scale: float = 1.0,
+                     sinks=None, workspace, out, lse, stream=None) -> None:
+    """Balanced plans: the decode kernel over the work list in ``workspace``."""
+    lib = load_library()
+    if block_table_stride is None:
+        block_table_stride = block_table.stride(0) if block_table is not None else 0
+    _check("mla_decode_items", lib.mla_decode_items(
+        ctypes.byref(plan), _ptr(q), _ptr(kv_cache), _ptr(block_table), int(block_table_stride),
+        _ptr(seq_lens), _ptr(qo_indptr), _ptr(sparse_slots), _ptr(sparse_indptr),
+        float(softmax_scale), float(q_scale), float(kv_scale), _ptr(sinks), _ptr(workspace),
+        _ws_bytes(workspace), _ptr(out), _ptr(lse), _stream(stream)))
+
+
+def mla_merge_items(plan: Plan, *, qo_indptr=None, sinks=None, workspace, out, lse,
+                    stream=None) -> None:
+    """Balanced plans: out and lse of the split rows from their partials."""
+    lib = load_library()
+    _check("mla_merge_items", lib.mla_merge_items(
+        ctypes.byref(plan), _ptr(qo_indptr), _ptr(sinks), _ptr(workspace), _ws_bytes(workspace),
+        _ptr(out), _ptr(lse), _stream(stream)))
 
 
 def mla_decode_segments(plan: Plan, q, kv_cache, *, block_table=None, block_table_stride=None,

@@ -151,6 +151,25 @@ dim3 grid_of(const mla_plan_t* plan) {
               static_cast<unsigned>(plan->grid_z));
 }
 
+// Workspace pieces of the balanced schedule (after the status block):
+// the item count, the items (32 bytes each), the unit table, then the
+// partial slots at the plan's segm_* offsets.
+struct SchedLayout {
+  size_t n_items, items, unit_tab, end;
+};
+
+SchedLayout sched_layout(const mla_plan_t* plan) {
+  const mla_problem_t& p = plan->prob;
+  const size_t units = static_cast<size_t>(p.topk > 0 ? p.num_tokens : p.num_reqs);
+  SchedLayout l;
+  l.n_items = kWsAlign;
+  l.items = 2 * kWsAlign;
+  l.unit_tab = l.items + align_up(static_cast<size_t>(plan->max_items) * 32, kWsAlign);
+  l.end = l.unit_tab + align_up(units * static_cast<size_t>(plan->row_tiles) * 8, kWsAlign);
+  return l;
+}
+
+// d.items selects the balanced grid: one CTA pair per item slot.
 mla_status_t launch_decode(const mla_plan_t* plan, const mla::DecodeParams& d, int* status,
                            cudaStream_t stream) {
   if (plan->grid_z == 0) return MLA_OK;
@@ -158,11 +177,87 @@ mla_status_t launch_decode(const mla_plan_t* plan, const mla::DecodeParams& d, i
   if (plan->kernel == mla::kTcPair128) {
     const int64_t q_rows = static_cast<int64_t>(p.num_tokens) * p.num_heads;
     const int64_t kv_rows = static_cast<int64_t>(p.num_blocks) * p.block_size;
+    const dim3 grid = d.items != nullptr ? dim3(2u * static_cast<unsigned>(plan->max_items), 1u, 1u)
+                                         : grid_of(plan);
     return cuda_status(mla::launch_decode_tc(d, p.kv_dtype == MLA_DTYPE_FP8_E4M3, q_rows, kv_rows,
-                                             grid_of(plan), status, stream));
+                                             grid, status, stream));
   }
   return cuda_status(mla::launch_decode_mma(plan->kernel, p.kv_dtype == MLA_DTYPE_FP8_E4M3, d,
                                             grid_of(plan), stream));
+}
+
+// ---- balanced schedule stages (plan->schedule == 1)
+
+mla::SchedParams sched_params(const mla_plan_t* plan, const Inputs& in, uint8_t* ws) {
+  const mla_problem_t& p = plan->prob;
+  const SchedLayout l = sched_layout(plan);
+  mla::SchedParams sp{};
+  sp.seq_lens = in.seq_lens;
+  sp.qo_indptr = in.qo_indptr;
+  sp.slot_indptr = p.topk > 0 ? in.slot_indptr : nullptr;
+  sp.topk = p.topk;
+  sp.sparse = p.topk > 0 ? 1 : 0;
+  sp.num_units = p.topk > 0 ? p.num_tokens : p.num_reqs;
+  sp.num_heads = p.num_heads;
+  sp.tiles_max = plan->row_tiles;
+  sp.split_cap = plan->split_items;
+  sp.items = reinterpret_cast<int32_t*>(ws + l.items);
+  sp.n_items = reinterpret_cast<int32_t*>(ws + l.n_items);
+  sp.unit_tab = reinterpret_cast<int32_t*>(ws + l.unit_tab);
+  return sp;
+}
+
+mla_status_t check_scheduled(const mla_plan_t* plan, const void* workspace, size_t workspace_bytes) {
+  if (plan == nullptr || plan->schedule != 1) return MLA_ERR_INVALID_ARG;
+  if (plan->kernel != mla::kTcPair128 || plan->max_items <= 0 || plan->split_items <= 0 ||
+      plan->row_tiles <= 0)
+    return MLA_ERR_INVALID_ARG;
+  if (workspace == nullptr || workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE;
+  if (!aligned(workspace, kWsAlign)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+mla_status_t run_schedule(const mla_plan_t* plan, const Inputs& in, uint8_t* ws, cudaStream_t stream) {
+  return cuda_status(mla::launch_schedule(sched_params(plan, in, ws), stream));
+}
+
+mla_status_t run_items(const mla_plan_t* plan, const Inputs& in, const float* sinks, uint8_t* ws,
+                       void* out, float* lse, cudaStream_t stream) {
+  const mla::SchedParams sp = sched_params(plan, in, ws);
+  mla::DecodeParams d = make_params(plan, in);
+  d.items = sp.items;
+  d.n_items = sp.n_items;
+  d.final_mode = 0;
+  d.sinks = sinks;
+  d.out = out;
+  d.lse = lse;
+  d.segm_out = reinterpret_cast<float*>(ws + plan->segm_output_offset);
+  d.segm_max = reinterpret_cast<float*>(ws + plan->segm_max_offset);
+  d.segm_expsum = reinterpret_cast<float*>(ws + plan->segm_expsum_offset);
+  return launch_decode(plan, d, reinterpret_cast<int*>(ws + plan->status_offset), stream);
+}
+
+mla_status_t run_merge_items(const mla_plan_t* plan, const Inputs& in, const float* sinks, uint8_t* ws,
+                             void* out, float* lse, cudaStream_t stream) {
+  const mla_problem_t& p = plan->prob;
+  const mla::SchedParams sp = sched_params(plan, in, ws);
+  mla::MergeParams m{};
+  m.segm_out = reinterpret_cast<float*>(ws + plan->segm_output_offset);
+  m.segm_max = reinterpret_cast<float*>(ws + plan->segm_max_offset);
+  m.segm_expsum = reinterpret_cast<float*>(ws + plan->segm_expsum_offset);
+  m.part = part_lens_for(plan, in);
+  m.num_tokens = p.num_tokens;
+  m.num_heads = p.num_heads;
+  m.num_segments = 1;
+  m.rank = kRank;
+  m.tile_size = plan->tile_size;
+  m.sinks = sinks;
+  m.out = out;
+  m.lse = lse;
+  m.unit_tab = sp.unit_tab;
+  m.tiles_max = plan->row_tiles;
+  m.sparse = sp.sparse;
+  return cuda_status(mla::launch_merge(m, stream));
 }
 
 }  // namespace
@@ -226,25 +321,13 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   const int32_t max_len = sparse ? p.topk : p.max_seq_len;
 
   int32_t ns = p.num_segments;
-  if (ns == 0 && use_tc) {
-    // One CTA pair per two SMs, one pair per (row tile, segment, unit).
-    // Estimated time in 64-key chunks: waves of pairs, each as long as the
-    // longest possible segment plus a fixed per-pair cost (~8 chunks:
-    // q load, pipeline fill, the output write) and, for NS > 1, the merge's
-    // extra pass over the partials (~1 chunk per segment).
-    const int64_t items_per_seg = static_cast<int64_t>(units > 0 ? units : 1) * row_tiles;
-    const int64_t pairs = sms / 2 > 0 ? sms / 2 : 1;
-    int64_t best = -1;
-    for (int32_t cand = 1; cand <= 16; ++cand) {
-      const int64_t waves = (items_per_seg * cand + pairs - 1) / pairs;
-      const int64_t span = static_cast<int64_t>(cand) * tile;
-      const int64_t seg_keys = (max_len + span - 1) / span * tile;
-      const int64_t cost = waves * (8 + (seg_keys + 63) / 64) + (cand > 1 ? cand : 0);
-      if (best < 0 || cost < best) {
-        best = cost;
-        ns = cand;
-      }
-    }
+  // The tensor-core kernel with the planner's choice of segments takes the
+  // balanced schedule: segment lengths follow the device-resident lengths
+  // (sched.cu), at most two items per CTA pair when anything is split.
+  const int64_t unit_tiles = static_cast<int64_t>(units) * row_tiles;
+  const bool balanced = ns == 0 && use_tc && unit_tiles <= (1 << 20);
+  if (balanced || (ns == 0 && use_tc)) {
+    ns = 1;
   } else if (ns == 0) {
     // Enough CTAs for about two per SM, but no segment shorter than
     // ~512 keys: each extra segment costs a partial write and read.
@@ -266,7 +349,20 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   plan->grid_z = units;
   plan->status_offset = 0;
   plan->workspace_bytes = kWsAlign;
-  if (ns > 1) {
+  if (balanced) {
+    const int32_t split_cap = 2 * (sms / 2 > 0 ? sms / 2 : 1);
+    plan->schedule = 1;
+    plan->split_items = split_cap;
+    plan->max_items = static_cast<int32_t>(unit_tiles + split_cap / 2);  // rows + cuts
+    const SchedLayout l = sched_layout(plan);
+    const size_t slot_rows = static_cast<size_t>(split_cap) * 128;
+    const size_t out_b = align_up(slot_rows * kRank * sizeof(float), kWsAlign);
+    const size_t max_b = align_up(slot_rows * sizeof(float), kWsAlign);
+    plan->segm_output_offset = l.end;
+    plan->segm_max_offset = l.end + out_b;
+    plan->segm_expsum_offset = l.end + out_b + max_b;
+    plan->workspace_bytes = l.end + out_b + 2 * max_b;
+  } else if (ns > 1) {
     const size_t th = static_cast<size_t>(p.num_tokens) * p.num_heads;
     const size_t out_b = align_up(th * ns * kRank * sizeof(float), kWsAlign);
     const size_t max_b = align_up(th * ns * sizeof(float), kWsAlign);
@@ -324,6 +420,12 @@ mla_status_t mla_decode_fwd(const mla_plan_t* plan, const void* q, const void* k
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* status = reinterpret_cast<int*>(ws + plan->status_offset);
   mla::DecodeParams d = make_params(plan, in);
+  if (plan->schedule == 1) {
+    s = run_schedule(plan, in, ws, stream);
+    if (s == MLA_OK) s = run_items(plan, in, sinks, ws, out, lse, stream);
+    if (s == MLA_OK) s = run_merge_items(plan, in, sinks, ws, out, lse, stream);
+    return s;
+  }
   if (plan->num_segments == 1) {
     d.final_mode = 1;
     d.sinks = sinks;
@@ -351,6 +453,67 @@ mla_status_t mla_decode_fwd(const mla_plan_t* plan, const void* q, const void* k
   m.out = out;
   m.lse = lse;
   return cuda_status(mla::launch_merge(m, stream));
+}
+
+mla_status_t mla_decode_schedule(const mla_plan_t* plan, const int32_t* seq_lens,
+                                 const int32_t* qo_indptr, const int32_t* sparse_indptr,
+                                 void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  mla_status_t s = check_scheduled(plan, workspace, workspace_bytes);
+  if (s != MLA_OK) return s;
+  s = check_problem(plan->prob);
+  if (s != MLA_OK) return s;
+  const mla_problem_t& p = plan->prob;
+  if (p.num_tokens == 0) return MLA_OK;
+  if (p.topk == 0) {
+    if (seq_lens == nullptr || !aligned(seq_lens, 4)) return MLA_ERR_INVALID_ARG;
+    if (p.max_qlen > 1 && qo_indptr == nullptr) return MLA_ERR_INVALID_ARG;
+  }
+  Inputs in{};
+  in.seq_lens = seq_lens;
+  in.qo_indptr = p.topk > 0 ? nullptr : qo_indptr;
+  in.slot_indptr = p.topk > 0 ? sparse_indptr : nullptr;
+  return run_schedule(plan, in, static_cast<uint8_t*>(workspace), stream);
+}
+
+mla_status_t mla_decode_items(const mla_plan_t* plan, const void* q, const void* kv_cache,
+                              const int32_t* block_table, int64_t block_table_stride,
+                              const int32_t* seq_lens, const int32_t* qo_indptr,
+                              const int32_t* sparse_slots, const int32_t* sparse_indptr,
+                              float softmax_scale, float q_scale, float kv_scale,
+                              const float* sinks, void* workspace, size_t workspace_bytes,
+                              void* out, float* lse, cudaStream_t stream) {
+  const Inputs in{q, kv_cache, block_table, block_table_stride, seq_lens, qo_indptr,
+                  sparse_slots, sparse_indptr, softmax_scale, q_scale, kv_scale};
+  mla_status_t s = check_scheduled(plan, workspace, workspace_bytes);
+  if (s != MLA_OK) return s;
+  s = check_inputs(plan, in);
+  if (s != MLA_OK) return s;
+  const mla_problem_t& p = plan->prob;
+  if ((sinks != nullptr) != (p.has_sinks == 1)) return MLA_ERR_INVALID_ARG;
+  if (p.num_tokens == 0) return MLA_OK;
+  if (out == nullptr || lse == nullptr || !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (sinks != nullptr && !aligned(sinks, 4)) return MLA_ERR_INVALID_ARG;
+  return run_items(plan, in, sinks, static_cast<uint8_t*>(workspace), out, lse, stream);
+}
+
+mla_status_t mla_merge_items(const mla_plan_t* plan, const int32_t* qo_indptr, const float* sinks,
+                             void* workspace, size_t workspace_bytes, void* out, float* lse,
+                             cudaStream_t stream) {
+  mla_status_t s = check_scheduled(plan, workspace, workspace_bytes);
+  if (s != MLA_OK) return s;
+  s = check_problem(plan->prob);
+  if (s != MLA_OK) return s;
+  const mla_problem_t& p = plan->prob;
+  if ((sinks != nullptr) != (p.has_sinks == 1)) return MLA_ERR_INVALID_ARG;
+  if (p.num_tokens == 0) return MLA_OK;
+  if (p.topk == 0 && p.max_qlen > 1 && qo_indptr == nullptr) return MLA_ERR_INVALID_ARG;
+  if (out == nullptr || lse == nullptr || !aligned(out, 16) || !aligned(lse, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (sinks != nullptr && !aligned(sinks, 4)) return MLA_ERR_INVALID_ARG;
+  Inputs in{};
+  in.qo_indptr = p.topk > 0 ? nullptr : qo_indptr;
+  return run_merge_items(plan, in, sinks, static_cast<uint8_t*>(workspace), out, lse, stream);
 }
 
 mla_status_t mla_merge_segments(const float* segm_output, const float* segm_max,

@@ -131,6 +131,8 @@ struct Ctx {
   int H, tok0, qlen, row0, rows_total, part_len;
   int64_t list_base;
   int seg, seg_start, seg_end, n_chunks, unit;
+  int pslot;  // balanced schedule: partial slot of this piece, -1 = write out/lse
+  bool fin;   // write the output (else base-2 partials)
   __device__ uint32_t bar(int i) const { return bar0 + 8u * i; }
   __device__ uint32_t peer_bar(int i) const { return peer + kOffBar + 8u * i; }
 };
@@ -242,8 +244,14 @@ __device__ void score_ring_tma(const Ctx& x, const TcMaps& maps, const DecodePar
       }
       const uint32_t dst = smem_u32(x.smem + C::kOffRing + slot * kSlot);
       mbar_arrive_expect_tx(x.bar(kRFull + slot), two ? kSlot : kBox);
-      tma_load_2d(dst, &maps.kv, C::kBoxCols * j, row0, x.bar(kRFull + slot));
-      if (two) tma_load_2d(dst + kBox, &maps.kv, C::kBoxCols * j, row1, x.bar(kRFull + slot));
+      if (j == C::kBoxesK - 1) {  // the rope columns: their only read
+        const uint64_t pol = l2_evict_first();
+        tma_load_2d_hint(dst, &maps.kv, C::kBoxCols * j, row0, x.bar(kRFull + slot), pol);
+        if (two) tma_load_2d_hint(dst + kBox, &maps.kv, C::kBoxCols * j, row1, x.bar(kRFull + slot), pol);
+      } else {  // latent columns, read again by the value CTA
+        tma_load_2d(dst, &maps.kv, C::kBoxCols * j, row0, x.bar(kRFull + slot));
+        if (two) tma_load_2d(dst + kBox, &maps.kv, C::kBoxCols * j, row1, x.bar(kRFull + slot));
+      }
     }
   }
   // every load this warp issued must have landed before the CTA exits
@@ -287,8 +295,11 @@ __device__ void score_ring_gather(const Ctx& x, const TcMaps& maps, const Decode
       }
       if (lane == 0) mbar_arrive_expect_tx(x.bar(kRFull + slot), kSlot);
       __syncwarp();
-      tma_gather4(smem_u32(x.smem + C::kOffRing + slot * kSlot + 512 * lane), &maps.kv1, 64 * j, r[0], r[1],
-                  r[2], r[3], x.bar(kRFull + slot));
+      const uint32_t dst = smem_u32(x.smem + C::kOffRing + slot * kSlot + 512 * lane);
+      if (j == C::kBoxesK - 1)  // the rope columns: their only read
+        tma_gather4_hint(dst, &maps.kv1, 64 * j, r[0], r[1], r[2], r[3], x.bar(kRFull + slot), l2_evict_first());
+      else
+        tma_gather4(dst, &maps.kv1, 64 * j, r[0], r[1], r[2], r[3], x.bar(kRFull + slot));
     }
   }
   // every gather this warp issued must have landed before the CTA exits
@@ -315,9 +326,11 @@ __device__ void value_stage_tma(const Ctx& x, const TcMaps& maps, const DecodePa
       break;
     const int row = cache_row(p, bt_row, x.seg_start + c * kKeys);
     mbar_arrive_expect_tx(x.bar(kVFull + st), nbox * kBox);
+    // the value columns' last read: first out of L2
+    const uint64_t pol = l2_evict_first();
     for (int j = pidx; j < C::kBoxesV; j += C::kProdV)
-      tma_load_2d(smem_u32(x.smem + C::kOffV + (st * C::kBoxesV + j) * kBox), &maps.kv,
-                  C::kBoxCols * j, row, x.bar(kVFull + st));
+      tma_load_2d_hint(smem_u32(x.smem + C::kOffV + (st * C::kBoxesV + j) * kBox), &maps.kv,
+                       C::kBoxCols * j, row, x.bar(kVFull + st), pol);
     issued = c + 1;
   }
   for (int c = max(0, issued - C::kStagesV); c < issued; ++c)
@@ -361,8 +374,8 @@ __device__ void value_stage_gather(const Ctx& x, const TcMaps& maps, const Decod
       for (int k = 0; k < 4; ++k) r[k] = r[k] >= 0 ? r[k] : sub;
       if (lane == 0) mbar_arrive_expect_tx(x.bar(kVFull + st), 2 * kBox);
       __syncwarp();
-      tma_gather4(smem_u32(stage + jbox * kBox + 512 * (lane & 15)), &maps.kv1, 64 * jbox, r[0], r[1], r[2],
-                  r[3], x.bar(kVFull + st));
+      tma_gather4_hint(smem_u32(stage + jbox * kBox + 512 * (lane & 15)), &maps.kv1, 64 * jbox, r[0], r[1],
+                       r[2], r[3], x.bar(kVFull + st), l2_evict_first());  // last read of these rows
     } else {
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
       for (int b = 0; b < 2; ++b)
@@ -579,7 +592,7 @@ __device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
     const int64_t th = static_cast<int64_t>(tok) * H + head;
     float mult;
     float lse = -INFINITY;
-    if (p.final_mode) {
+    if (x.fin) {
       if (p.sinks != nullptr) {
         const float s2 = p.sinks[head] * kLog2e;
         const float M = fmaxf(m_ref, s2);
@@ -597,10 +610,11 @@ __device__ void score_softmax(const Ctx& x, const DecodeParams& p) {
       mult = l > 0.f ? 1.f / l : 0.f;
     }
     if (row_ok) {
-      if (p.final_mode) {
+      if (x.fin) {
         p.lse[th] = lse;
       } else {
-        const int64_t ts = th * p.num_segments + x.seg;
+        const int64_t ts = x.pslot >= 0 ? static_cast<int64_t>(x.pslot) * kRows + r
+                                        : th * p.num_segments + x.seg;
         p.segm_max[ts] = l > 0.f ? m_true : -INFINITY;
         p.segm_expsum[ts] = l > 0.f ? l * exp2f(m_ref - m_true) : 0.f;
       }
@@ -752,9 +766,10 @@ __device__ void value_rows(const Ctx& x, const DecodeParams& p) {
       rbase[it] = nullptr;
       if (rr < x.rows_total) {
         const int64_t th = static_cast<int64_t>(x.tok0 + rr / H) * H + rr % H;
-        rbase[it] = p.final_mode
-                        ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + th * kRank)
-                        : reinterpret_cast<uint4*>(p.segm_out + (th * p.num_segments + x.seg) * kRank);
+        const int64_t ts = x.pslot >= 0 ? static_cast<int64_t>(x.pslot) * kRows + (rr - x.row0)
+                                        : th * p.num_segments + x.seg;
+        rbase[it] = x.fin ? reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + th * kRank)
+                          : reinterpret_cast<uint4*>(p.segm_out + ts * kRank);
       }
     }
     // one 32-row x 128-byte tile: this lane's row in, four rows per store out
@@ -775,21 +790,21 @@ __device__ void value_rows(const Ctx& x, const DecodeParams& p) {
 #pragma unroll 1
     for (int g = 0; g < 8; ++g) {
       // 16-byte units of column group g: 8 per bf16 row piece, 16 per fp32
-      const int gu = p.final_mode ? 8 * g : 16 * g;
+      const int gu = x.fin ? 8 * g : 16 * g;
       if (n == 0) {  // no key: zeros, written straight out (coalesced)
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int it = 0; it < 8; ++it) {
           if (rbase[it] == nullptr) continue;
           rbase[it][gu + qc] = z;
-          if (!p.final_mode) rbase[it][gu + 8 + qc] = z;
+          if (!x.fin) rbase[it][gu + 8 + qc] = z;
         }
         continue;
       }
       uint32_t o[64];
       tmem_ld_32x32b_x64(x.tbase + lane_off + kTmemO + 64 * g, o);
       tmem_ld_wait();
-      if (p.final_mode) {
+      if (x.fin) {
         uint32_t w[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -870,9 +885,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
   x.lane = x.tid & 31;
   const uint32_t crank = cluster_ctarank();
   const bool score = crank == 0;
-  const int tile = blockIdx.x >> 1;
-  x.seg = blockIdx.y;
-  x.unit = blockIdx.z;
+  int tile, item_begin = 0, item_end = 0;
+  x.pslot = -1;
+  if (p.items != nullptr) {
+    // balanced schedule: both CTAs of the pair read the same item, once the
+    // grid that wrote the list (launched just before) has completed
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // the merge grid may launch once every CTA of this one has started (it
+    // waits for this grid to complete before it reads)
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const int item = blockIdx.x >> 1;
+    if (item >= *p.n_items) return;
+    const int4 a = reinterpret_cast<const int4*>(p.items)[2 * item];
+    const int4 b = reinterpret_cast<const int4*>(p.items)[2 * item + 1];
+    x.unit = a.x;
+    tile = a.y;
+    item_begin = a.z;
+    item_end = a.w;
+    x.pslot = b.x;
+    x.seg = 0;
+    x.fin = x.pslot < 0;
+  } else {
+    tile = blockIdx.x >> 1;
+    x.seg = blockIdx.y;
+    x.unit = blockIdx.z;
+    x.fin = p.final_mode != 0;
+  }
   x.H = p.num_heads;
 
   x.qlen = 1;
@@ -898,11 +936,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
   x.row0 = tile * kRows;
   if (x.row0 >= x.rows_total) return;  // both CTAs of the pair take this branch together
 
-  const int span = p.num_segments * p.tile_size;
-  const int tps = x.part_len > 0 ? cdiv(x.part_len, span) : 0;
-  const int seg_len = tps * p.tile_size;
-  x.seg_start = x.seg * seg_len;
-  x.seg_end = min(x.seg_start + seg_len, x.part_len);
+  if (p.items != nullptr) {
+    x.seg_start = item_begin;
+    x.seg_end = min(item_end, x.part_len);
+  } else {
+    const int span = p.num_segments * p.tile_size;
+    const int tps = x.part_len > 0 ? cdiv(x.part_len, span) : 0;
+    const int seg_len = tps * p.tile_size;
+    x.seg_start = x.seg * seg_len;
+    x.seg_end = min(x.seg_start + seg_len, x.part_len);
+  }
   x.n_chunks = x.seg_end > x.seg_start ? cdiv(x.seg_end - x.seg_start, kKeys) : 0;
 
   x.bar0 = smem_u32(smem + kOffBar);
@@ -1044,8 +1087,23 @@ cudaError_t launch_variant(const TcMaps& maps, const DecodeParams& p, dim3 grid,
     if (e != cudaSuccess) return e;
     done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  decode_tc_kernel<FP8, SPARSE><<<grid, C::kThreads, C::kSmem, stream>>>(maps, p, status);
-  return cudaGetLastError();
+  if (p.items == nullptr) {
+    decode_tc_kernel<FP8, SPARSE><<<grid, C::kThreads, C::kSmem, stream>>>(maps, p, status);
+    return cudaGetLastError();
+  }
+  // balanced schedule: programmatic dependent launch, so that the grid is
+  // set up while the schedule kernel before it runs
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<FP8, SPARSE>, maps, p, status);
 }
 
 }  // namespace

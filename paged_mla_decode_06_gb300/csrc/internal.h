@@ -35,7 +35,26 @@ struct DecodeParams {
   float* segm_expsum;            // [T, H, NS]
   void* out;                     // [T, H, 512] bf16
   float* lse;                    // [T, H]
+  // balanced schedule (tensor-core kernel): item i = blockIdx.x / 2 is
+  // {unit, tile, key begin, key end, partial slot or -1 (write out/lse)}
+  // at items[8 i ..]; null selects the uniform NS partition
+  const int32_t* items;
+  const int32_t* n_items;
 };
+
+// Balanced work list (sched.cu).
+struct SchedParams {
+  const int32_t* seq_lens;       // dense [R]
+  const int32_t* qo_indptr;      // dense [R+1] or null
+  const int32_t* slot_indptr;    // sparse [T+1] or null (topk per token)
+  int32_t topk, sparse, num_units, num_heads, tiles_max;
+  int32_t split_cap;             // item budget when segments are split
+  int32_t* items;                // [max_items, 8]
+  int32_t* n_items;              // [1]
+  int32_t* unit_tab;             // [num_units * tiles_max, 2]: first partial slot (-1), pieces
+};
+
+cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
 
 // Where the merge finds each token's partition length.
 struct PartLens {
@@ -57,6 +76,11 @@ struct MergeParams {
   const float* sinks;
   void* out;     // bf16
   float* lse;
+  // balanced schedule: partials live in slots of 128 rows; unit_tab gives
+  // each (unit, row tile) its first slot and piece count (null: uniform NS)
+  const int32_t* unit_tab;
+  int32_t tiles_max;
+  int32_t sparse;
 };
 
 struct LseMergeParams {

@@ -4,6 +4,9 @@
 // One warp per (token, head). The token's partition length and the tile size
 // give the segments that exist (start < len, tiles_per_segment =
 // cdiv(len, NS * tile)); of those, segments with expsum > 0 contribute.
+// Under the balanced schedule the row's pieces come from the unit table
+// instead, and rows whose unit was not split are left as the decode kernel
+// wrote them.
 // Pass 1 reads the base-2 maxima, pass 2 streams each live segment's
 // normalised output coalesced (lane i reads float4 i, i + 32, ...) and
 // accumulates it with weight l_s * 2^(m2_s - M). The sink logit, when given,
@@ -12,24 +15,27 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "merge_row.cuh"
 
 namespace mla {
 namespace {
 
 constexpr int kWarpsPerBlock = 4;
 
+// Request of token t: the last r with qo_indptr[r] <= t.
+__device__ __forceinline__ int request_of(const PartLens& pl, int t) {
+  int lo = 0, hi = pl.num_reqs - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pl.qo_indptr[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  return lo;
+}
+
 __device__ __forceinline__ int part_len_of(const PartLens& pl, int t) {
   switch (pl.mode) {
     case 0: return pl.lens[t];
-    case 1: {
-      if (pl.qo_indptr == nullptr) return pl.seq_lens[t];
-      int lo = 0, hi = pl.num_reqs - 1;  // last request r with qo_indptr[r] <= t
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (pl.qo_indptr[mid] <= t) lo = mid; else hi = mid - 1;
-      }
-      return pl.seq_lens[lo];
-    }
+    case 1: return pl.qo_indptr == nullptr ? pl.seq_lens[t] : pl.seq_lens[request_of(pl, t)];
     case 2: return pl.indptr[t + 1] - pl.indptr[t];
     default: return pl.constant;
   }
@@ -37,65 +43,42 @@ __device__ __forceinline__ int part_len_of(const PartLens& pl, int t) {
 
 template <int VPL>  // float4 values per lane: rank / 128
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeParams p) {
+  // launched as a programmatic dependent of the decode under the balanced
+  // schedule: wait for it to complete (a no-op after an ordinary launch)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_heads;
   if (gw >= total) return;
   const int t = static_cast<int>(gw / p.num_heads);
   const int h = static_cast<int>(gw % p.num_heads);
+  const float sink2 = p.sinks != nullptr ? p.sinks[h] * kLog2e : -INFINITY;
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + gw * p.rank;
+  if (p.unit_tab != nullptr) {
+    // balanced schedule: the rows of a (unit, 128-row tile) split into k > 1
+    // pieces own k consecutive slots of 128 rows; k == 1 rows were written
+    // by the decode kernel itself
+    int u = t, tok0 = t;
+    if (!p.sparse && p.part.qo_indptr != nullptr) {
+      u = request_of(p.part, t);
+      tok0 = p.part.qo_indptr[u];
+    }
+    const int r = (t - tok0) * p.num_heads + h;
+    if (r / 128 >= p.tiles_max) return;
+    const int2 e = reinterpret_cast<const int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + r / 128];
+    if (e.y <= 1) return;
+    merge_row<VPL, true>(p.segm_out, p.segm_max, p.segm_expsum, static_cast<int64_t>(e.x) * 128 + r % 128,
+                         128, e.y, sink2, out, p.lse + gw, lane);
+    return;
+  }
   const int NS = p.num_segments;
   const int len = part_len_of(p.part, t);
   const int span = NS * p.tile_size;
   const int tps = len > 0 ? cdiv(len, span) : 0;
   const int seg = tps * p.tile_size;
   const int live = len > 0 ? min(NS, cdiv(len, seg)) : 0;
-  const int64_t base = gw * NS;
-
-  float M = -INFINITY;
-  for (int s = 0; s < live; ++s) {
-    if (p.segm_expsum[base + s] > 0.f) M = fmaxf(M, p.segm_max[base + s]);
-  }
-  const bool has_sink = p.sinks != nullptr;
-  const float sink2 = has_sink ? p.sinks[h] * kLog2e : -INFINITY;
-  M = fmaxf(M, sink2);
-
-  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + gw * p.rank;
-  if (M == -INFINITY) {
-#pragma unroll
-    for (int v = 0; v < VPL; ++v)
-      *reinterpret_cast<uint2*>(out + (v * 32 + lane) * 4) = make_uint2(0u, 0u);
-    if (lane == 0) p.lse[gw] = -INFINITY;
-    return;
-  }
-  float acc[VPL][4];
-#pragma unroll
-  for (int v = 0; v < VPL; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
-  float W = 0.f;
-  for (int s = 0; s < live; ++s) {
-    const float l = p.segm_expsum[base + s];
-    if (!(l > 0.f)) continue;
-    const float w = l * exp2f(p.segm_max[base + s] - M);
-    W += w;
-    const float4* src = reinterpret_cast<const float4*>(p.segm_out + (base + s) * p.rank);
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      const float4 x = __ldg(src + v * 32 + lane);
-      acc[v][0] += w * x.x;
-      acc[v][1] += w * x.y;
-      acc[v][2] += w * x.z;
-      acc[v][3] += w * x.w;
-    }
-  }
-  if (has_sink) W += exp2f(sink2 - M);
-  const float inv = 1.f / W;
-#pragma unroll
-  for (int v = 0; v < VPL; ++v) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[v][0] * inv, acc[v][1] * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[v][2] * inv, acc[v][3] * inv);
-    *reinterpret_cast<uint2*>(out + (v * 32 + lane) * 4) =
-        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-  }
-  if (lane == 0) p.lse[gw] = kLn2 * (M + log2f(W));
+  merge_row<VPL, false>(p.segm_out, p.segm_max, p.segm_expsum, gw * NS, 1, live, sink2, out, p.lse + gw,
+                        lane);
 }
 
 // Natural-log (out, lse) pairs of W key shards of the same rows: weights
@@ -174,6 +157,21 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t warps = static_cast<int64_t>(p.num_tokens) * p.num_heads;
   if (warps == 0) return cudaSuccess;
   const unsigned blocks = static_cast<unsigned>((warps + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  if (p.unit_tab != nullptr) {
+    // balanced schedule: programmatic dependent launch after the decode, so
+    // that the grid is in place when the decode completes
+    if (p.rank != 512) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(blocks, 1, 1);
+    cfg.blockDim = dim3(kWarpsPerBlock * 32, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, merge_kernel<4>, p);
+  }
   switch (p.rank / 128) {
     case 1: merge_kernel<1><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(p); break;
     case 2: merge_kernel<2><<<blocks, kWarpsPerBlock * 32, 0, stream>>>(p); break;

@@ -1,0 +1,231 @@
+// sched.cu -- the balanced work list of the tensor-core decode: split-K
+// segments sized per batch from the device-resident lengths, so that every
+// CTA pair gets about the same number of keys (a planner that fills the
+// SMs). The "rocm_aiter_mla_sparse" page's ROCMAiterMLASparseImpl._forward_mla
+// hands its decode call such a list (work_indptr, reduce_indptr,
+// reduce_partial_map) on its persistent path.
+//
+// One block of 256 threads. A row is a (unit, row tile) pair, a unit being
+// a request of the dense variant or a token of the sparse one; a row covers
+// the unit's g = cdiv(len, 128) key groups. The rows are laid end to end
+// (unit-major) and the sequence of all their groups is cut every W =
+// cdiv(total, pairs) groups, as if each CTA pair took the next W groups;
+// a cut closer than W / 8 to either end of its row is dropped, so that no
+// piece is a sliver. Every row thus becomes k >= 1 pieces (one, of size 0,
+// for an empty row, whose rows still get zeros and -inf). Items are written
+// longest first: CTA pairs are handed out in launch order, so the pairs that
+// finish early take the short pieces (longest-processing-time list
+// scheduling). Pieces of a split row write base-2 partials to consecutive
+// partial slots; the unit table gives each row its first slot and its piece
+// count, from which the merge finds them. Cuts number
+// fewer than the pairs, so the slots of split rows number at most two per
+// pair and the items at most rows + pairs.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mla {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kGroupKeys = 128;   // piece boundaries fall on 128-key groups
+constexpr int kSizeBins = 2048;   // ranking bins of piece sizes (in groups)
+constexpr int kCacheUnits = 2048; // units whose sizes are kept in shared memory
+
+struct UnitInfo {
+  int groups;
+  int tiles;
+};
+
+__device__ __forceinline__ UnitInfo unit_info_global(const SchedParams& p, int u) {
+  int len, qlen = 1;
+  if (p.sparse) {
+    len = p.slot_indptr != nullptr ? p.slot_indptr[u + 1] - p.slot_indptr[u] : p.topk;
+  } else {
+    len = p.seq_lens[u];
+    if (p.qo_indptr != nullptr) qlen = p.qo_indptr[u + 1] - p.qo_indptr[u];
+  }
+  UnitInfo i;
+  i.groups = len > 0 ? cdiv(len, kGroupKeys) : 0;
+  const int64_t rows = static_cast<int64_t>(qlen > 0 ? qlen : 0) * p.num_heads;
+  const int64_t tiles = (rows + 127) / 128;
+  i.tiles = static_cast<int>(tiles < p.tiles_max ? tiles : p.tiles_max);
+  return i;
+}
+
+// Block-wide sum over one value per thread.
+__device__ long long block_sum(long long v, long long* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  long long s = 0;
+  for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+  return s;
+}
+
+// Exclusive prefix of v over the block (thread order); *total gets the sum.
+__device__ long long block_exclusive_scan(long long v, long long* red, long long* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const long long n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  __syncthreads();
+  if (lane == 31) red[warp] = inc;
+  __syncthreads();
+  long long before = 0, all = 0;
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const long long s = red[w];
+    if (w < warp) before += s;
+    all += s;
+  }
+  *total = all;
+  return before + inc - v;
+}
+
+// Cuts of the row occupying groups [a, a + g) of the sequence: multiples of
+// W strictly inside, none within W / 8 of either end. Returns their number
+// and the first one.
+struct Cuts {
+  long long first;
+  int count;
+};
+
+__device__ __forceinline__ Cuts row_cuts(long long a, int g, long long W) {
+  const long long d = W / 8;
+  const long long lo = a + d + 1, hi = a + g - d - 1;  // allowed cut positions
+  Cuts c{0, 0};
+  if (g > 0 && hi >= lo) {
+    c.first = (lo + W - 1) / W * W;
+    if (c.first <= hi) c.count = static_cast<int>((hi - c.first) / W + 1);
+  }
+  return c;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams p) {
+  // the decode kernel may launch now; it waits for this grid before reading
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+  __shared__ long long red[kThreads / 32];
+  __shared__ int hist[kSizeBins];
+  __shared__ int start[kSizeBins];
+  __shared__ int cache_g[kCacheUnits];
+  __shared__ int cache_t[kCacheUnits];
+  const int tid = threadIdx.x;
+  const int U = p.num_units;
+  const bool cached = U <= kCacheUnits;
+  auto info = [&](int u) -> UnitInfo {
+    if (cached) return UnitInfo{cache_g[u], cache_t[u]};
+    return unit_info_global(p, u);
+  };
+
+  // total groups over all rows
+  long long total = 0;
+  for (int u = tid; u < U; u += kThreads) {
+    const UnitInfo i = unit_info_global(p, u);
+    if (cached) {
+      cache_g[u] = i.groups;
+      cache_t[u] = i.tiles;
+    }
+    total += static_cast<long long>(i.tiles) * i.groups;
+  }
+  total = block_sum(total, red);  // (its barriers also publish the cache)
+  const long long pairs = p.split_cap / 2 > 0 ? p.split_cap / 2 : 1;
+  const long long W = total > 0 ? (total + pairs - 1) / pairs : 1;
+
+  // piece-size histogram; rows of unit u start at pos_u (unit-major)
+  for (int b = tid; b < kSizeBins; b += kThreads) hist[b] = 0;
+  long long carry = 0;
+  for (int u0 = 0; u0 < U; u0 += kThreads) {
+    const int u = u0 + tid;
+    UnitInfo i{0, 0};
+    if (u < U) i = info(u);
+    long long sum;
+    const long long pos = carry + block_exclusive_scan(static_cast<long long>(i.tiles) * i.groups, red, &sum);
+    carry += sum;
+    for (int t = 0; t < i.tiles; ++t) {
+      const long long a = pos + static_cast<long long>(t) * i.groups;
+      const Cuts c = row_cuts(a, i.groups, W);
+      long long prev = a;
+      for (int j = 0; j <= c.count; ++j) {
+        const long long next = j < c.count ? c.first + j * W : a + i.groups;
+        atomicAdd(&hist[static_cast<int>(min(next - prev, static_cast<long long>(kSizeBins - 1)))], 1);
+        prev = next;
+      }
+    }
+  }
+  __syncthreads();
+  // start[b] = number of pieces in bins above b (kBinsPer bins per thread,
+  // thread 0 taking the largest)
+  {
+    constexpr int kBinsPer = kSizeBins / kThreads;
+    const int top = kSizeBins - 1 - kBinsPer * tid;
+    int mine = 0;
+#pragma unroll
+    for (int j = 0; j < kBinsPer; ++j) mine += hist[top - j];
+    long long all;
+    int before = static_cast<int>(block_exclusive_scan(mine, red, &all));
+#pragma unroll
+    for (int j = 0; j < kBinsPer; ++j) {
+      start[top - j] = before;
+      before += hist[top - j];
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < kSizeBins; b += kThreads) hist[b] = 0;  // now the per-bin cursor
+  __syncthreads();
+
+  // items, unit table and partial slots (slots of split rows, row order)
+  carry = 0;
+  long long slot_carry = 0, n_items = 0;
+  for (int u0 = 0; u0 < U; u0 += kThreads) {
+    const int u = u0 + tid;
+    UnitInfo i{0, 0};
+    if (u < U) i = info(u);
+    long long sum;
+    const long long pos = carry + block_exclusive_scan(static_cast<long long>(i.tiles) * i.groups, red, &sum);
+    carry += sum;
+    int nslots = 0;
+    for (int t = 0; t < i.tiles; ++t) {
+      const Cuts c = row_cuts(pos + static_cast<long long>(t) * i.groups, i.groups, W);
+      if (c.count > 0) nslots += c.count + 1;
+    }
+    long long slot_sum;
+    int slot = static_cast<int>(slot_carry + block_exclusive_scan(nslots, red, &slot_sum));
+    slot_carry += slot_sum;
+    for (int t = 0; t < i.tiles; ++t) {
+      const long long a = pos + static_cast<long long>(t) * i.groups;
+      const Cuts c = row_cuts(a, i.groups, W);
+      const int k = c.count + 1;
+      const int pbase = k > 1 ? slot : -1;
+      reinterpret_cast<int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + t] = make_int2(pbase, k);
+      long long prev = a;
+      for (int j = 0; j < k; ++j) {
+        const long long next = j < c.count ? c.first + j * W : a + i.groups;
+        const int bin = static_cast<int>(min(next - prev, static_cast<long long>(kSizeBins - 1)));
+        const int at = start[bin] + atomicAdd(&hist[bin], 1);
+        int4* it = reinterpret_cast<int4*>(p.items) + 2 * static_cast<int64_t>(at);
+        const long long kb = (prev - a) * kGroupKeys, ke = (next - a) * kGroupKeys;
+        it[0] = make_int4(u, t, static_cast<int>(min(kb, static_cast<long long>(INT32_MAX))),
+                          static_cast<int>(min(ke, static_cast<long long>(INT32_MAX))));
+        it[1] = make_int4(k > 1 ? pbase + j : -1, 0, 0, 0);
+        prev = next;
+      }
+      n_items += k;
+      if (k > 1) slot += k;
+    }
+  }
+  n_items = block_sum(n_items, red);
+  if (tid == 0) *p.n_items = static_cast<int32_t>(n_items);
+}
+
+}  // namespace
+
+cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream) {
+  schedule_kernel<<<1, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

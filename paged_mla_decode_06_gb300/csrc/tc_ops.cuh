@@ -130,6 +130,21 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int 
       "l"(tmap), "r"(x), "r"(y), "r"(bar)
       : "memory");
 }
+// L2 policy for data read for the last time (evicted before other lines).
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(pol));
+  return pol;
+}
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap, int x, int y, uint32_t bar,
+                                                 uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol)
+      : "memory");
+}
 // Four rows r0..r3 of a 2-D tensor whose map has a one-row box, each the
 // box's width from column x, to consecutive rows of the destination
 // (swizzled as the map says); completes on the CTA's own barrier.
@@ -139,6 +154,15 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const void* tmap, int 
       "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];\n" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
+// tma_gather4 with an L2 cache policy.
+__device__ __forceinline__ void tma_gather4_hint(uint32_t dst, const void* tmap, int x, int r0, int r1, int r2,
+                                                 int r3, uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;\n" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar), "l"(pol)
       : "memory");
 }
 // Pull a box of a 2-D tensor into L2 only (no shared memory, no barrier).

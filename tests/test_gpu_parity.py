@@ -189,6 +189,76 @@ def test_tcgen05_head_counts_and_short_rows(heads):
     assert_close(out, lse, ref_o, ref_l, "bf16", f"tcgen05 H={heads}", tol=TOL_FEW_KEYS)
 
 
+@pytest.mark.parametrize("case", ["dense", "multi_token", "sparse"])
+def test_balanced_schedule_items(case):
+    """The planner's balanced schedule (tensor-core kernel, segments left to
+    the planner): read the work list back from the workspace and check that
+    the pieces of every (unit, row tile) cover its key groups once and in
+    order, items come longest first, split pieces own distinct partial slots
+    within the budget, the items fit the grid, the output matches the oracle,
+    and a second decode and merge over the same list give the same bits."""
+    if case == "dense":
+        w = I.build_dense(71, seq_lens=[0, 1, 129, 700, 3000, 9000, 257], num_heads=128,
+                          block_size=64, num_segments=0)
+        lens, tiles = w.seq_lens, np.ones(w.num_reqs, dtype=np.int64)
+    elif case == "multi_token":
+        w = I.build_dense(72, seq_lens=[5000, 40, 2600], num_heads=128, block_size=64,
+                          qlens=[4, 1, 3], with_sinks=True, num_segments=0)
+        q = np.diff(w.qo_indptr)
+        lens, tiles = w.seq_lens, -(-q * 128 // 128)
+    else:
+        w = I.sparse_topk(num_reqs=2, tokens_per_req=3, cache_tokens=4096, topk=1024,
+                          max_pad=300, num_segments=0)
+        lens, tiles = np.full(w.num_tokens, 1024), np.ones(w.num_tokens, dtype=np.int64)
+    out, lse, dw = run_gpu(w, kernel=B.MLA_KERNEL_TCGEN05)
+    plan = dw.plan
+    assert plan.schedule == 1 and plan.num_segments == 1
+    ws = dw.workspace.cpu().numpy()
+    n = int(ws[256:260].view(np.int32)[0])
+    items = ws[512:512 + 32 * n].view(np.int32).reshape(n, 8)
+    tab_off = 512 + -(-plan.max_items * 32 // 256) * 256
+    tab = ws[tab_off:tab_off + 8 * len(lens) * plan.row_tiles].view(np.int32).reshape(
+        len(lens), plan.row_tiles, 2)
+    sizes = (items[:, 3] - items[:, 2]) // 128
+    assert np.all(np.diff(sizes) <= 0), "items not longest first"
+    split = False
+    slots = []
+    for u in range(len(lens)):
+        g = -(-int(lens[u]) // 128)
+        for t in range(int(tiles[u])):
+            mine = items[(items[:, 0] == u) & (items[:, 1] == t)]
+            mine = mine[np.argsort(mine[:, 2])]
+            k = len(mine)
+            assert k == max(1, tab[u, t, 1]) and k >= 1
+            assert mine[0, 2] == 0 and mine[-1, 3] == g * 128
+            assert np.array_equal(mine[1:, 2], mine[:-1, 3])
+            if k > 1:
+                split = True
+                assert sorted(mine[:, 4].tolist()) == list(range(tab[u, t, 0], tab[u, t, 0] + k))
+                slots += mine[:, 4].tolist()
+            else:
+                assert mine[0, 4] == -1 and tab[u, t, 0] == -1
+    assert n == sum(max(1, int(tab[u, t, 1])) for u in range(len(lens)) for t in range(int(tiles[u])))
+    assert len(set(slots)) == len(slots) and all(0 <= s < plan.split_items for s in slots)
+    assert n <= plan.max_items
+    assert split or case == "sparse" or n == sum(int(t) for t in tiles)
+    ref_o, ref_l = run_oracle(w)
+    assert_close(out, lse, ref_o, ref_l, "bf16", f"balanced {case}", tol=TOL_FEW_KEYS)
+    # the same work list serves a second decode: identical bits
+    dw.out.zero_()
+    dw.lse.zero_()
+    B.mla_decode_items(plan, dw.q, dw.cache, block_table=None if w.sparse else dw.block_table,
+                       seq_lens=None if w.sparse else dw.seq_lens, qo_indptr=dw.qo_indptr,
+                       sparse_slots=dw.slots, softmax_scale=w.softmax_scale, sinks=dw.sinks,
+                       workspace=dw.workspace, out=dw.out, lse=dw.lse)
+    B.mla_merge_items(plan, qo_indptr=dw.qo_indptr, sinks=dw.sinks, workspace=dw.workspace,
+                      out=dw.out, lse=dw.lse)
+    torch.cuda.synchronize()
+    assert dw.status() == 0
+    assert np.array_equal(dw.out.float().cpu().numpy(), out)
+    assert np.array_equal(dw.lse.cpu().numpy(), lse)
+
+
 def test_tcgen05_segment_partials():
     w = I.build_dense(61, seq_lens=[1, 70, 300, 1000], num_heads=128, block_size=64,
                       num_segments=4)
