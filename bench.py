@@ -114,8 +114,8 @@ def _flops(w):
 # kernel, from one ncu capture (the profile summary under profiles/ names the
 # command and the numbers), valid only for the kernel source it was taken on.
 PROFILED_TRAFFIC = {
-    "source_sha256": "f0983620a3a657f3a3088cbd1fb3b5ee9f17b3dccb51d5c68c168f52cc1ef5f0",
-    "dram_per_alg_byte": (139.019520 + 3.561728) / 138.103440,
+    "source_sha256": "bfeec0978352d4f062be786030ff111c91ed26cd15b393c83e44c77050794297",
+    "dram_per_alg_byte": (139.576320 + 3.362560) / 138.103440,
 }
 
 
