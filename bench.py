@@ -119,11 +119,12 @@ PROFILED_TRAFFIC = {
 }
 
 
-def _profiled_traffic(alg_bytes, kernel_id):
+def _profiled_traffic(alg_bytes, kernel_id, workload_name):
     """DRAM bytes of one launch scaled from the capture, or None once the
-    kernel source differs from the one profiled (or for another kernel)."""
+    kernel source differs from the one profiled, for another kernel, or for
+    a workload other than the captured one (the DeepSeek-V3-shaped batch)."""
     import hashlib
-    if kernel_id != 4:
+    if kernel_id != 4 or workload_name != "dsv3":
         return None
     src = os.path.join(ROOT, "paged_mla_decode_06_gb300", "csrc", "decode_tc.cu")
     try:
@@ -481,7 +482,7 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
                          "frac": achieved / peak_bw,
-                         "traffic": _profiled_traffic(alg, int(plan.kernel)),
+                         "traffic": _profiled_traffic(alg, int(plan.kernel), args.workload),
                          "kernel": kname,
                          "kernel_us": dms * 1e3, "algorithmic_bytes": alg,
                          "peak_source": f"hbm_gbs of {src}",
