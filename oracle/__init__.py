@@ -9,5 +9,6 @@ from .mla_oracle import (  # noqa: F401
     attend, concat_quant_q, decode_bf16, decode_e4m3fn, encode_e4m3fn, dense_slots, dequantize, index_convert,
     merge_lse_shards, merge_segments, mla_decode, partition_lengths, round_robin_positions,
     segment_bounds,
-    segment_partials, tile_size_for_block, token_layout, visible_len,
+    segment_partials, tile_size_for_block, token_layout, visible_len, sparse_seqlen,
+    fit_kpool_indices,
 )

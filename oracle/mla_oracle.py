@@ -1,5 +1,6 @@
 """Plain fp64 CPU oracle for paged MLA decode, segment partials, the segment
-merge and the sparse index conversion.
+merge, the sparse index conversion and the sparse front end (list lengths,
+fixed-width index fit).
 
 TEST INFRASTRUCTURE. Only the tests, ``__graft_entry__.smoke()`` and the
 CPU-baseline leg of ``bench.py`` may import or run anything in this package.
@@ -379,6 +380,61 @@ def index_convert(req_id, block_table, token_indices, block_size, cu_seqlens=Non
     for t in range(T):
         n = int(cu[t + 1] - cu[t])
         out[cu[t]:cu[t] + n] = conv[t, :n]
+    return out
+
+
+# ---------------------------------------------------------------------------
+# sparse front end: per-token list lengths and the fixed-width index fit
+# ---------------------------------------------------------------------------
+
+def sparse_seqlen(query_start_loc, seq_lens, topk):
+    """Per-token length of the sparse slot list and its exclusive prefix sum
+    (the sparse page's metadata builder: ``generate_sparse_seqlen_triton``
+    then ``torch.cumsum`` into ``paged_kv_indptr``).
+
+    Reading (the kernel body is not on the page): token ``j`` of request
+    ``r`` (``qlen = qsl[r + 1] - qsl[r]`` tokens) sees the causal prefix
+    ``[0, seq_len - qlen + j]``, as the dense page's
+    ``dcp_local_verify_row_lens`` has it, and can select at most ``topk`` of
+    those positions: ``len = clamp(seq_len - qlen + j + 1, 0, topk)``.
+    Returns ``(lens [T], indptr [T + 1])`` as int64.
+    """
+    qsl = np.asarray(query_start_loc, dtype=np.int64)
+    sl = np.asarray(seq_lens, dtype=np.int64)
+    T = int(qsl[-1])
+    lens = np.zeros(T, dtype=np.int64)
+    for r in range(len(sl)):
+        qlen = int(qsl[r + 1] - qsl[r])
+        for j in range(qlen):
+            lens[qsl[r] + j] = min(max(int(sl[r]) - qlen + j + 1, 0), int(topk))
+    indptr = np.zeros(T + 1, dtype=np.int64)
+    indptr[1:] = np.cumsum(lens)
+    return lens, indptr
+
+
+def fit_kpool_indices(token_indices, topk):
+    """Fit ``[T, W]`` top-k rows (``W >= topk``) to AITER's fixed width
+    ``topk`` (``fit_kpool_indices_to_aiter`` on the sparse page, which does
+    so while keeping the kpool tail's live entries).
+
+    Reading (the kernel body is not on the page): columns ``[0, topk)`` are
+    the selected positions, columns ``[topk, W)`` the kpool tail; a tail
+    entry is live when it is ``>= 0``. With ``n`` the number of live tail
+    entries (at most ``topk`` of them, the first ones, are kept), the output
+    row is the first ``topk - n`` selected entries followed by the ``n``
+    live tail entries in their order. Nothing is de-duplicated. ``W ==
+    topk`` returns the rows unchanged; ``W < topk`` is an error.
+    """
+    ti = np.asarray(token_indices, dtype=np.int64)
+    T, W = ti.shape
+    if W < topk:
+        raise ValueError("token_indices width must be at least topk")
+    out = np.empty((T, topk), dtype=np.int64)
+    for t in range(T):
+        live = [int(v) for v in ti[t, topk:] if v >= 0][:topk]
+        n = len(live)
+        out[t, :topk - n] = ti[t, :topk - n]
+        out[t, topk - n:] = live
     return out
 
 

@@ -521,3 +521,68 @@ def test_concat_quant_q():
     assert q.shape == (2, 3, 576) and np.array_equal(q[..., :512], a) and np.array_equal(q[..., 512:], b)
     codes = O.concat_quant_q(a, b, q_scale=0.05)
     np.testing.assert_allclose(O.decode_e4m3fn(codes) * 0.05, q, rtol=0.07, atol=0.05 * 2 ** -9)
+
+
+# ---------------------------------------------------------------- sparse front end
+
+def test_sparse_seqlen_golden():
+    rows = _golden_rows("sparse_seqlen.txt")
+    want_lens = [int(v) for v in rows[0][1:]]
+    want_indptr = [int(v) for v in rows[1][1:]]
+    seq = [5, 300, 2, 0, 130]
+    qlens = [1, 3, 2, 1, 4]
+    qsl = np.concatenate([[0], np.cumsum(qlens)])
+    lens, indptr = O.sparse_seqlen(qsl, seq, 128)
+    assert lens.tolist() == want_lens
+    assert indptr.tolist() == want_indptr
+
+
+def test_sparse_seqlen_matches_dense_visible_rows():
+    # the same causal bound as the dense multi-token rows, capped at topk
+    rng = np.random.default_rng(21)
+    seq = rng.integers(0, 700, size=40)
+    qlens = rng.integers(1, 5, size=40)
+    qsl = np.concatenate([[0], np.cumsum(qlens)])
+    for topk in (128, 512, 2048):
+        lens, indptr = O.sparse_seqlen(qsl, seq, topk)
+        assert indptr[0] == 0 and np.array_equal(np.diff(indptr), lens)
+        t = 0
+        for r in range(40):
+            for j in range(int(qlens[r])):
+                assert lens[t] == min(O.visible_len(int(seq[r]), int(qlens[r]), j), topk)
+                t += 1
+        # within a request consecutive tokens see one more position each
+        for r in range(40):
+            seg = lens[qsl[r]:qsl[r + 1]]
+            assert np.all(np.diff(seg) <= 1) and np.all(np.diff(seg) >= 0)
+            assert np.all((seg >= 0) & (seg <= topk))
+
+
+def test_fit_kpool_golden():
+    rows = [" ".join(r) for r in _golden_rows("fit_kpool.txt")]
+    for line in rows:
+        a, b = line.split("|")
+        row = np.array([int(v) for v in a.split()])
+        want = [int(v) for v in b.split()]
+        got = O.fit_kpool_indices(row[None, :], 4)
+        assert got[0].tolist() == want, line
+
+
+def test_fit_kpool_invariants_and_edges():
+    rng = np.random.default_rng(22)
+    T, topk, W = 50, 128, 192
+    ti = rng.integers(0, 10000, size=(T, W))
+    ti[rng.random((T, W)) < 0.3] = -1
+    out = O.fit_kpool_indices(ti, topk)
+    assert out.shape == (T, topk)
+    for t in range(T):
+        live = [v for v in ti[t, topk:] if v >= 0]
+        n = len(live)
+        assert out[t, topk - n:].tolist() == live           # every live tail entry, in order
+        assert out[t, :topk - n].tolist() == ti[t, :topk - n].tolist()  # a prefix of the selection
+    # width == topk: unchanged; width < topk: error; more live tail than topk: the first topk
+    assert np.array_equal(O.fit_kpool_indices(ti[:, :topk], topk), ti[:, :topk])
+    with pytest.raises(ValueError):
+        O.fit_kpool_indices(ti[:, :100], topk)
+    wide = np.concatenate([np.full((2, 4), 7), np.arange(12).reshape(2, 6)], axis=1)
+    assert O.fit_kpool_indices(wide, 4).tolist() == [[0, 1, 2, 3], [6, 7, 8, 9]]

@@ -50,6 +50,23 @@ def _convert_no_oob(req, bt, ti, bs, cu_seqlens=None, out_init=None):
     return np.where(ti >= 0, base * bs + np.where(ti >= 0, ti % bs, 0), -1)
 
 
+def _seqlen_without_own_token(qsl, seq, topk):
+    qsl = np.asarray(qsl, dtype=np.int64)
+    lens = []
+    for r in range(len(seq)):
+        q = int(qsl[r + 1] - qsl[r])
+        lens += [min(max(int(seq[r]) - q + j, 0), topk) for j in range(q)]
+    lens = np.array(lens, dtype=np.int64)
+    return lens, np.concatenate([[0], np.cumsum(lens)])
+
+
+def _fit_keeps_whole_tail(ti, topk):
+    ti = np.asarray(ti, dtype=np.int64)
+    tail = ti[:, topk:][:, :topk]
+    n = tail.shape[1]
+    return np.concatenate([ti[:, :topk - n], tail], axis=1)
+
+
 _orig_attend = M.attend
 _orig_merge = M.merge_segments
 
@@ -61,6 +78,8 @@ CASES = [
     ("segment_bounds", _bounds_floor, P.test_segment_partition_golden),
     ("merge_segments", _merge_wrong_base, P.test_merge_single_segment_is_identity),
     ("index_convert", _convert_no_oob, P.test_index_convert_brute_force_and_edges),
+    ("sparse_seqlen", _seqlen_without_own_token, P.test_sparse_seqlen_golden),
+    ("fit_kpool_indices", _fit_keeps_whole_tail, P.test_fit_kpool_golden),
 ]
 
 
