@@ -292,6 +292,47 @@ MLA_API mla_status_t mla_merge_segments(const float* segm_output, const float* s
                                 int32_t out_dtype, void* out, float* lse, cudaStream_t stream);
 
 /*
+ * mla_sparse_seqlen -- per-token lengths of the sparse slot lists and their
+ * exclusive prefix sum, ready to serve as cu_seqlens of
+ * mla_sparse_index_convert and sparse_indptr of the decode ([sparse]
+ * ROCMAiterMLASparseMetadataBuilder.build: generate_sparse_seqlen_triton,
+ * then the cumsum into paged_kv_indptr). The page gives no kernel body; the
+ * reading taken: token j of request r (qlen = query_start_loc[r + 1] -
+ * query_start_loc[r] tokens) sees its causal prefix (the bound of [dense]
+ * dcp_local_verify_row_lens) and selects at most topk positions:
+ *   lens[t] = clamp(seq_lens[r] - qlen + j + 1, 0, topk).
+ * Tokens at or past query_start_loc[num_reqs] get length 0.
+ *   query_start_loc [num_reqs + 1] int32, nondecreasing; seq_lens [num_reqs]
+ *   lens [num_tokens] int32 or NULL; indptr [num_tokens + 1] int32
+ * One block on `stream`. Errors: MLA_ERR_INVALID_ARG for negative sizes,
+ * topk <= 0, NULL or misaligned pointers; MLA_ERR_UNSUPPORTED when
+ * num_tokens * topk exceeds INT32_MAX.
+ */
+MLA_API mla_status_t mla_sparse_seqlen(const int32_t* query_start_loc, const int32_t* seq_lens,
+                                       int32_t num_reqs, int32_t num_tokens, int32_t topk,
+                                       int32_t* lens, int32_t* indptr, cudaStream_t stream);
+
+/*
+ * mla_fit_kpool_indices -- the indexer's [T, width] rows (width >= topk)
+ * fitted to the fixed width topk ([sparse] fit_kpool_indices_to_aiter,
+ * which keeps the kpool tail's live entries). The page gives no kernel
+ * body; the reading taken: columns [0, topk) are the selected positions,
+ * columns [topk, width) the kpool tail, an entry is live when >= 0; with n
+ * the number of live tail entries (the first topk of them at most), output
+ * row t is the first topk - n selected entries followed by the n live tail
+ * entries in their order. Nothing is de-duplicated; width == topk copies.
+ *   token_indices [T, width] int32, row stride ti_row_stride (>= width)
+ *   out [T, topk] int32, row stride out_row_stride (>= topk), not
+ *   overlapping the input
+ * One warp per row. Errors: MLA_ERR_INVALID_ARG for width < topk, topk <= 0,
+ * short strides, NULL, misaligned or overlapping buffers.
+ */
+MLA_API mla_status_t mla_fit_kpool_indices(const int32_t* token_indices, int64_t ti_row_stride,
+                                           int32_t num_tokens, int32_t width, int32_t topk,
+                                           int32_t* out, int64_t out_row_stride,
+                                           cudaStream_t stream);
+
+/*
  * mla_sparse_index_convert -- per-request top-k positions to global slots
  * ([sparse] triton_convert_req_index_to_global_index):
  *   out[t, i] = block_table[req_id[t], idx / block_size] * block_size

@@ -106,6 +106,12 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                                  ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                  _vp, _vp, _vp]
         lib.mla_sparse_index_convert.restype = st
+        lib.mla_sparse_seqlen.argtypes = [_vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                          _vp, _vp, _vp]
+        lib.mla_sparse_seqlen.restype = st
+        lib.mla_fit_kpool_indices.argtypes = [_vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                              ctypes.c_int32, _vp, ctypes.c_int64, _vp]
+        lib.mla_fit_kpool_indices.restype = st
         lib.mla_merge_lse.argtypes = [_vp, _vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                       ctypes.c_int32, _vp, _vp, _vp, _vp]
         lib.mla_merge_lse.restype = st
@@ -291,6 +297,27 @@ def mla_concat_quant_q(ql_nope, q_pe, *, out, q_scale: float | None = None, stre
         _ptr(ql_nope), ql_nope.stride(0), ql_nope.stride(1), _ptr(q_pe), q_pe.stride(0),
         q_pe.stride(1), T, H, MLA_DTYPE_FP8_E4M3 if fp8 else MLA_DTYPE_BF16,
         float(q_scale) if fp8 else 1.0, _ptr(out), _stream(stream)))
+
+
+def mla_sparse_seqlen(query_start_loc, seq_lens, *, topk: int, indptr, lens=None,
+                      stream=None) -> None:
+    """Per-token sparse list lengths (``lens``, optional) and their exclusive
+    prefix sum (``indptr``, ``[T + 1]``)."""
+    lib = load_library()
+    num_reqs = query_start_loc.numel() - 1
+    num_tokens = indptr.numel() - 1
+    _check("mla_sparse_seqlen", lib.mla_sparse_seqlen(
+        _ptr(query_start_loc), _ptr(seq_lens), num_reqs, num_tokens, int(topk), _ptr(lens),
+        _ptr(indptr), _stream(stream)))
+
+
+def mla_fit_kpool_indices(token_indices, *, topk: int, out, stream=None) -> None:
+    """``[T, W]`` top-k rows fitted to width ``topk`` into ``out [T, topk]``."""
+    lib = load_library()
+    T, W = token_indices.shape
+    _check("mla_fit_kpool_indices", lib.mla_fit_kpool_indices(
+        _ptr(token_indices), token_indices.stride(0), T, W, int(topk), _ptr(out), out.stride(0),
+        _stream(stream)))
 
 
 def mla_sparse_index_convert(req_id, block_table, token_indices, *, block_size: int,

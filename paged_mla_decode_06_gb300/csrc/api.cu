@@ -607,6 +607,37 @@ mla_status_t mla_concat_quant_q(const void* ql_nope, int64_t nope_stride_t, int6
   return cuda_status(mla::launch_concat_q(q, stream));
 }
 
+mla_status_t mla_sparse_seqlen(const int32_t* query_start_loc, const int32_t* seq_lens,
+                               int32_t num_reqs, int32_t num_tokens, int32_t topk, int32_t* lens,
+                               int32_t* indptr, cudaStream_t stream) {
+  if (num_reqs < 0 || num_tokens < 0 || topk <= 0) return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_tokens) * topk > INT32_MAX) return MLA_ERR_UNSUPPORTED;
+  if (indptr == nullptr || !aligned(indptr, 4)) return MLA_ERR_INVALID_ARG;
+  if (lens != nullptr && !aligned(lens, 4)) return MLA_ERR_INVALID_ARG;
+  if (query_start_loc == nullptr || !aligned(query_start_loc, 4)) return MLA_ERR_INVALID_ARG;
+  if (num_reqs > 0 && (seq_lens == nullptr || !aligned(seq_lens, 4))) return MLA_ERR_INVALID_ARG;
+  return cuda_status(mla::launch_sparse_seqlen(query_start_loc, seq_lens, num_reqs, num_tokens, topk, lens,
+                                               indptr, stream));
+}
+
+mla_status_t mla_fit_kpool_indices(const int32_t* token_indices, int64_t ti_row_stride,
+                                   int32_t num_tokens, int32_t width, int32_t topk, int32_t* out,
+                                   int64_t out_row_stride, cudaStream_t stream) {
+  if (num_tokens < 0 || topk <= 0 || width < topk) return MLA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return MLA_OK;
+  if (token_indices == nullptr || out == nullptr || !aligned(token_indices, 4) || !aligned(out, 4))
+    return MLA_ERR_INVALID_ARG;
+  if (ti_row_stride < width || out_row_stride < topk) return MLA_ERR_INVALID_ARG;
+  // the output must not overlap the input rows
+  const uintptr_t in0 = reinterpret_cast<uintptr_t>(token_indices);
+  const uintptr_t in1 = in0 + static_cast<uintptr_t>((num_tokens - 1) * ti_row_stride + width) * 4;
+  const uintptr_t o0 = reinterpret_cast<uintptr_t>(out);
+  const uintptr_t o1 = o0 + static_cast<uintptr_t>((num_tokens - 1) * out_row_stride + topk) * 4;
+  if (o0 < in1 && in0 < o1) return MLA_ERR_INVALID_ARG;
+  return cuda_status(mla::launch_fit_kpool(token_indices, ti_row_stride, num_tokens, width, topk, out,
+                                           out_row_stride, stream));
+}
+
 mla_status_t mla_sparse_index_convert(const int32_t* req_id, const int32_t* block_table,
                                       int32_t bt_rows, int32_t bt_cols, int64_t bt_row_stride,
                                       const int32_t* token_indices, int64_t ti_row_stride,

@@ -115,6 +115,13 @@ cudaError_t launch_index_convert(const int32_t* req_id, const int32_t* block_tab
                                  int32_t num_tokens, int32_t topk, int32_t block_size,
                                  const int32_t* cu_seqlens, int32_t* out, cudaStream_t stream);
 
+// Sparse front end (sparse_front.cu).
+cudaError_t launch_sparse_seqlen(const int32_t* qsl, const int32_t* seq_lens, int32_t num_reqs,
+                                 int32_t num_tokens, int32_t topk, int32_t* lens, int32_t* indptr,
+                                 cudaStream_t stream);
+cudaError_t launch_fit_kpool(const int32_t* ti, int64_t ti_stride, int32_t num_tokens, int32_t width,
+                             int32_t topk, int32_t* out, int64_t out_stride, cudaStream_t stream);
+
 // tcgen05 CTA-pair kernel: q_rows / kv_rows are the row counts of the q
 // and cache tensors viewed as [rows, 576]; status (may be null) receives a
 // nonzero code if a bounded wait times out.

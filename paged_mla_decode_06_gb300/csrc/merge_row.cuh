@@ -33,7 +33,9 @@ template <int VPL, bool Coherent>
 __device__ void merge_row(const float* segm_out, const float* segm_max, const float* segm_expsum,
                           int64_t base, int64_t stride, int live, float sink2, __nv_bfloat16* out,
                           float* lse, int lane) {
+  // (unrolled so that the loads of several partials are in flight together)
   float M = -INFINITY;
+#pragma unroll 4
   for (int s = 0; s < live; ++s) {
     const int64_t i = base + s * stride;
     if (merge_load_f<Coherent>(segm_expsum + i) > 0.f) M = fmaxf(M, merge_load_f<Coherent>(segm_max + i));
@@ -50,6 +52,7 @@ __device__ void merge_row(const float* segm_out, const float* segm_max, const fl
 #pragma unroll
   for (int v = 0; v < VPL; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
   float W = 0.f;
+#pragma unroll 2
   for (int s = 0; s < live; ++s) {
     const int64_t i = base + s * stride;
     const float l = merge_load_f<Coherent>(segm_expsum + i);

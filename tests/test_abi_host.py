@@ -235,3 +235,73 @@ def test_concat_quant_q_rejects(lib):
     assert f(FAKE + 4, 512 * 8, 512, FAKE, 64 * 8, 64, 4, 8, 0, 1.0, FAKE, None) == B.MLA_ERR_INVALID_ARG
     assert f(None, 512 * 8, 512, FAKE, 64 * 8, 64, 4, 8, 0, 1.0, FAKE, None) == B.MLA_ERR_INVALID_ARG
     assert f(None, 0, 0, None, 0, 0, 0, 8, 0, 1.0, None, None) == B.MLA_OK
+
+
+# ---------------------------------------------------------------- balanced schedule
+
+def test_plan_balanced_schedule(lib):
+    plan = B.mla_decode_plan(_dense_problem())
+    assert plan.schedule == 1 and plan.num_segments == 1 and plan.kernel == 4
+    assert plan.split_items == 152 and plan.max_items == 64 + 76
+    slots_rows = plan.split_items * 128
+    assert plan.segm_output_offset % 256 == 0 and plan.segm_max_offset % 256 == 0
+    assert plan.segm_max_offset - plan.segm_output_offset >= slots_rows * 512 * 4
+    assert plan.segm_expsum_offset - plan.segm_max_offset >= slots_rows * 4
+    assert plan.workspace_bytes >= plan.segm_expsum_offset + slots_rows * 4
+    assert plan.workspace_bytes <= 64 << 20  # fits the static scratch of mla_decode_fwd_static
+    # an explicit segment count or the warp-MMA kernel keeps the uniform partition
+    assert B.mla_decode_plan(_dense_problem(num_segments=4)).schedule == 0
+    assert B.mla_decode_plan(_dense_problem(kernel=B.MLA_KERNEL_WARP_MMA)).schedule == 0
+
+
+def test_schedule_stages_reject_bad_arguments(lib):
+    plan = B.mla_decode_plan(_dense_problem())
+    uniform = B.mla_decode_plan(_dense_problem(num_segments=4))
+    wsb = plan.workspace_bytes
+    sched = lambda p, **k: lib.mla_decode_schedule(ctypes.byref(p), k.get("seq", FAKE), None, None,
+                                                   k.get("ws", FAKE), k.get("wsb", wsb), None)
+    assert sched(uniform) == B.MLA_ERR_INVALID_ARG
+    assert sched(plan, ws=None) == B.MLA_ERR_WORKSPACE
+    assert sched(plan, wsb=wsb - 1) == B.MLA_ERR_WORKSPACE
+    assert sched(plan, ws=FAKE + 64) == B.MLA_ERR_INVALID_ARG
+    assert sched(plan, seq=None) == B.MLA_ERR_INVALID_ARG
+    items = lambda p, **k: lib.mla_decode_items(
+        ctypes.byref(p), FAKE, FAKE, FAKE, 130, FAKE, None, None, None, 0.07, 1.0, 1.0, None,
+        k.get("ws", FAKE), k.get("wsb", wsb), k.get("out", FAKE), FAKE, None)
+    assert items(uniform) == B.MLA_ERR_INVALID_ARG
+    assert items(plan, wsb=16) == B.MLA_ERR_WORKSPACE
+    assert items(plan, out=None) == B.MLA_ERR_INVALID_ARG
+    merge = lambda p, **k: lib.mla_merge_items(ctypes.byref(p), None, k.get("sinks"), FAKE,
+                                               k.get("wsb", wsb), FAKE, FAKE, None)
+    assert merge(uniform) == B.MLA_ERR_INVALID_ARG
+    assert merge(plan, wsb=0) == B.MLA_ERR_WORKSPACE
+    assert merge(plan, sinks=FAKE) == B.MLA_ERR_INVALID_ARG   # sinks not announced
+
+
+# ---------------------------------------------------------------- sparse front end
+
+def test_sparse_seqlen_rejects_bad_arguments(lib):
+    f = lambda **k: lib.mla_sparse_seqlen(k.get("qsl", FAKE), k.get("seq", FAKE), k.get("R", 4),
+                                          k.get("T", 8), k.get("topk", 128), k.get("lens"),
+                                          k.get("indptr", FAKE), None)
+    assert f(topk=0) == B.MLA_ERR_INVALID_ARG
+    assert f(R=-1) == B.MLA_ERR_INVALID_ARG
+    assert f(indptr=None) == B.MLA_ERR_INVALID_ARG
+    assert f(indptr=FAKE + 2) == B.MLA_ERR_INVALID_ARG
+    assert f(qsl=None) == B.MLA_ERR_INVALID_ARG
+    assert f(seq=None) == B.MLA_ERR_INVALID_ARG
+    assert f(lens=FAKE + 1) == B.MLA_ERR_INVALID_ARG
+    assert f(T=1 << 20, topk=1 << 12) == B.MLA_ERR_UNSUPPORTED
+
+
+def test_fit_kpool_rejects_bad_arguments(lib):
+    f = lambda **k: lib.mla_fit_kpool_indices(k.get("ti", FAKE), k.get("tis", 320), k.get("T", 8),
+                                              k.get("W", 320), k.get("topk", 256),
+                                              k.get("out", FAKE + (1 << 20)), k.get("os", 256), None)
+    assert f(W=128) == B.MLA_ERR_INVALID_ARG          # width < topk
+    assert f(topk=0) == B.MLA_ERR_INVALID_ARG
+    assert f(tis=300) == B.MLA_ERR_INVALID_ARG        # row stride < width
+    assert f(os=200) == B.MLA_ERR_INVALID_ARG         # row stride < topk
+    assert f(out=FAKE + 64) == B.MLA_ERR_INVALID_ARG  # overlaps the input rows
+    assert f(ti=None) == B.MLA_ERR_INVALID_ARG
+    assert f(T=0) == B.MLA_OK                         # nothing to launch

@@ -189,7 +189,7 @@ def test_tcgen05_head_counts_and_short_rows(heads):
     assert_close(out, lse, ref_o, ref_l, "bf16", f"tcgen05 H={heads}", tol=TOL_FEW_KEYS)
 
 
-@pytest.mark.parametrize("case", ["dense", "multi_token", "sparse"])
+@pytest.mark.parametrize("case", ["dense", "multi_token", "sparse", "one_long"])
 def test_balanced_schedule_items(case):
     """The planner's balanced schedule (tensor-core kernel, segments left to
     the planner): read the work list back from the workspace and check that
@@ -206,6 +206,9 @@ def test_balanced_schedule_items(case):
                           qlens=[4, 1, 3], with_sinks=True, num_segments=0)
         q = np.diff(w.qo_indptr)
         lens, tiles = w.seq_lens, -(-q * 128 // 128)
+    elif case == "one_long":       # one request cut into pieces on every pair
+        w = I.build_dense(73, seq_lens=[60000], num_heads=128, block_size=64, num_segments=0)
+        lens, tiles = w.seq_lens, np.ones(1, dtype=np.int64)
     else:
         w = I.sparse_topk(num_reqs=2, tokens_per_req=3, cache_tokens=4096, topk=1024,
                           max_pad=300, num_segments=0)
@@ -524,3 +527,106 @@ def test_concat_quant_q_bit_exact(fp8):
         torch.cuda.synchronize()
         want = O.concat_quant_q(O.decode_bf16(nope), O.decode_bf16(pe))
         assert np.array_equal(out.float().cpu().numpy().astype(np.float64), want)
+
+
+# ---------------------------------------------------------------- sparse front end
+
+@pytest.mark.parametrize("topk", [128, 2048])
+def test_sparse_seqlen_bit_exact(topk):
+    rng = np.random.default_rng(topk)
+    R = 37
+    seq = rng.integers(0, 3 * topk, size=R).astype(np.int32)
+    seq[:3] = [0, 1, topk]
+    qlens = rng.integers(0, 5, size=R)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    T = int(qsl[-1]) + 2                   # two tokens past the last request: length 0
+    want_lens, want_ptr = O.sparse_seqlen(qsl, seq, topk)
+    want_lens = np.concatenate([want_lens, [0, 0]])
+    want_ptr = np.concatenate([want_ptr, [want_ptr[-1]] * 2])
+    dev = torch.device("cuda")
+    lens = torch.full((T,), -7, dtype=torch.int32, device=dev)
+    ptr = torch.full((T + 1,), -7, dtype=torch.int32, device=dev)
+    B.mla_sparse_seqlen(torch.from_numpy(qsl).to(dev), torch.from_numpy(seq).to(dev), topk=topk,
+                        indptr=ptr, lens=lens)
+    torch.cuda.synchronize()
+    assert np.array_equal(lens.cpu().numpy(), want_lens)
+    assert np.array_equal(ptr.cpu().numpy(), want_ptr)
+
+
+def test_sparse_seqlen_many_tokens():
+    rng = np.random.default_rng(5)
+    R = 3000
+    seq = rng.integers(0, 5000, size=R).astype(np.int32)
+    qlens = rng.integers(1, 5, size=R)
+    qsl = np.concatenate([[0], np.cumsum(qlens)]).astype(np.int32)
+    want_lens, want_ptr = O.sparse_seqlen(qsl, seq, 2048)
+    dev = torch.device("cuda")
+    ptr = torch.empty((int(qsl[-1]) + 1,), dtype=torch.int32, device=dev)
+    B.mla_sparse_seqlen(torch.from_numpy(qsl).to(dev), torch.from_numpy(seq).to(dev), topk=2048,
+                        indptr=ptr)
+    torch.cuda.synchronize()
+    assert np.array_equal(ptr.cpu().numpy(), want_ptr)
+
+
+@pytest.mark.parametrize("T,topk,W", [(33, 128, 128), (40, 256, 320), (7, 128, 700), (200, 2048, 2112)])
+def test_fit_kpool_bit_exact(T, topk, W):
+    rng = np.random.default_rng(T + W)
+    ti = rng.integers(0, 1 << 20, size=(T, W)).astype(np.int32)
+    ti[rng.random((T, W)) < 0.35] = -1
+    ti[0, topk:] = -1                      # no live tail
+    if W > topk:
+        ti[1, topk:] = np.arange(W - topk)  # every tail entry live
+    want = O.fit_kpool_indices(ti, topk)
+    dev = torch.device("cuda")
+    wide = torch.zeros((T, W + 5), dtype=torch.int32, device=dev)   # strided input
+    wide[:, :W] = torch.from_numpy(ti).to(dev)
+    out_wide = torch.full((T, topk + 3), 99, dtype=torch.int32, device=dev)
+    B.mla_fit_kpool_indices(wide[:, :W], topk=topk, out=out_wide[:, :topk])
+    torch.cuda.synchronize()
+    got = out_wide.cpu().numpy()
+    assert np.array_equal(got[:, :topk], want)
+    assert np.all(got[:, topk:] == 99)
+
+
+def test_sparse_front_end_pipeline():
+    """Indexer rows wider than topk -> fit -> per-token lengths -> ragged index
+    conversion -> decode over the ragged lists, against the same chain of
+    oracle functions."""
+    w = I.sparse_topk(num_reqs=3, tokens_per_req=3, cache_tokens=2048, topk=256, max_pad=0)
+    T, topk, W = w.num_tokens, 256, 256 + 48
+    rng = np.random.default_rng(31)
+    seq = np.array([100, 2048, 700], dtype=np.int32)
+    qsl = np.array([0, 3, 6, 9], dtype=np.int32)
+    ti = np.full((T, W), -1, dtype=np.int32)
+    for t in range(T):
+        r, j = t // 3, t % 3
+        vis = int(seq[r]) - 3 + j + 1
+        k = min(vis, topk)
+        ti[t, :k] = rng.choice(vis, size=k, replace=False)
+        tail = np.arange(max(0, vis - 40), vis)[::-1][:40]
+        ti[t, topk:topk + len(tail)] = tail
+        ti[t, topk + rng.integers(0, 48, size=10)] = -1
+    fitted = O.fit_kpool_indices(ti, topk)
+    lens, ptr = O.sparse_seqlen(qsl, seq, topk)
+    flat = O.index_convert(w.req_id_per_token, w.block_table, fitted, w.block_size, cu_seqlens=ptr,
+                           out_init=np.full(T * topk, -1, dtype=np.int64))[:int(ptr[-1])]
+    ref_o, ref_l = O.mla_decode(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, None, None, w.softmax_scale,
+                                sparse_slots=flat, sparse_indptr=ptr)
+    dw = B.DeviceWorkload(w, kernel=B.MLA_KERNEL_TCGEN05)
+    dev = dw.device
+    d_fit = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    B.mla_fit_kpool_indices(torch.from_numpy(ti).to(dev), topk=topk, out=d_fit)
+    d_ptr = torch.empty((T + 1,), dtype=torch.int32, device=dev)
+    B.mla_sparse_seqlen(torch.from_numpy(qsl).to(dev), torch.from_numpy(seq).to(dev), topk=topk,
+                        indptr=d_ptr)
+    d_flat = torch.full((T * topk,), -1, dtype=torch.int32, device=dev)
+    B.mla_sparse_index_convert(dw.req_id, dw.block_table, d_fit, block_size=w.block_size,
+                               cu_seqlens=d_ptr, out=d_flat)
+    B.mla_decode_fwd(dw.plan, dw.q, dw.cache, sparse_slots=d_flat, sparse_indptr=d_ptr,
+                     softmax_scale=w.softmax_scale, workspace=dw.workspace, out=dw.out, lse=dw.lse)
+    torch.cuda.synchronize()
+    assert dw.status() == 0
+    assert np.array_equal(d_ptr.cpu().numpy(), ptr)
+    assert np.array_equal(d_flat.cpu().numpy()[:int(ptr[-1])].astype(np.int64), flat)
+    assert_close(dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), ref_o, ref_l, "bf16",
+                 "sparse front end", tol=TOL_FEW_KEYS)
