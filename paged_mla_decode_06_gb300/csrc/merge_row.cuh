@@ -28,19 +28,30 @@ __device__ __forceinline__ float merge_load_f(const float* p) {
   else return __ldg(p);
 }
 
-// Rows of VPL * 128 values: lane i handles float4 i, i + 32, ...
+// Rows of VPL * 128 values: lane i handles float4 i, i + 32, ... . The
+// (max, expsum) pairs of the first kMeta partials are loaded together and
+// kept; the outputs of four partials at a time are loaded together, so that a
+// row costs about two memory round trips.
+constexpr int kMeta = 8;
+
 template <int VPL, bool Coherent>
 __device__ void merge_row(const float* segm_out, const float* segm_max, const float* segm_expsum,
                           int64_t base, int64_t stride, int live, float sink2, __nv_bfloat16* out,
                           float* lse, int lane) {
-  // (unrolled so that the loads of several partials are in flight together)
-  float M = -INFINITY;
-#pragma unroll 4
-  for (int s = 0; s < live; ++s) {
+  float lk[kMeta], mk[kMeta];
+#pragma unroll
+  for (int u = 0; u < kMeta; ++u) {
+    lk[u] = u < live ? merge_load_f<Coherent>(segm_expsum + base + u * stride) : 0.f;
+    mk[u] = u < live ? merge_load_f<Coherent>(segm_max + base + u * stride) : -INFINITY;
+  }
+  float M = sink2;
+#pragma unroll
+  for (int u = 0; u < kMeta; ++u)
+    if (lk[u] > 0.f) M = fmaxf(M, mk[u]);
+  for (int s = kMeta; s < live; ++s) {
     const int64_t i = base + s * stride;
     if (merge_load_f<Coherent>(segm_expsum + i) > 0.f) M = fmaxf(M, merge_load_f<Coherent>(segm_max + i));
   }
-  M = fmaxf(M, sink2);
   if (M == -INFINITY) {
 #pragma unroll
     for (int v = 0; v < VPL; ++v)
@@ -52,22 +63,40 @@ __device__ void merge_row(const float* segm_out, const float* segm_max, const fl
 #pragma unroll
   for (int v = 0; v < VPL; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
   float W = 0.f;
-#pragma unroll 2
-  for (int s = 0; s < live; ++s) {
-    const int64_t i = base + s * stride;
-    const float l = merge_load_f<Coherent>(segm_expsum + i);
-    if (!(l > 0.f)) continue;
-    const float w = l * exp2f(merge_load_f<Coherent>(segm_max + i) - M);
-    W += w;
-    const float4* src = reinterpret_cast<const float4*>(segm_out + i * (VPL * 128));
+  for (int s0 = 0; s0 < live; s0 += 4) {
+    float w[4];
 #pragma unroll
-    for (int v = 0; v < VPL; ++v) {
-      const float4 x = merge_load<Coherent>(src + v * 32 + lane);
-      acc[v][0] += w * x.x;
-      acc[v][1] += w * x.y;
-      acc[v][2] += w * x.z;
-      acc[v][3] += w * x.w;
+    for (int u = 0; u < 4; ++u) {
+      const int s = s0 + u;
+      float l = 0.f, m = 0.f;
+      if (s < kMeta) {
+#pragma unroll
+        for (int k = 0; k < kMeta; ++k)
+          if (k == s) { l = lk[k]; m = mk[k]; }
+      } else if (s < live) {
+        l = merge_load_f<Coherent>(segm_expsum + base + s * stride);
+        m = merge_load_f<Coherent>(segm_max + base + s * stride);
+      }
+      w[u] = l > 0.f ? l * exp2f(m - M) : 0.f;
+      W += w[u];
     }
+    float4 x[4][VPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float4* src = reinterpret_cast<const float4*>(segm_out + (base + (s0 + u) * stride) * (VPL * 128));
+#pragma unroll
+      for (int v = 0; v < VPL; ++v)
+        x[u][v] = w[u] != 0.f ? merge_load<Coherent>(src + v * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        acc[v][0] += w[u] * x[u][v].x;
+        acc[v][1] += w[u] * x[u][v].y;
+        acc[v][2] += w[u] * x[u][v].z;
+        acc[v][3] += w[u] * x[u][v].w;
+      }
   }
   if (sink2 != -INFINITY) W += exp2f(sink2 - M);
   const float inv = 1.f / W;

@@ -65,20 +65,21 @@ __device__ long long block_sum(long long v, long long* red) {
 }
 
 // Exclusive prefix of v over the block (thread order); *total gets the sum.
-__device__ long long block_exclusive_scan(long long v, long long* red, long long* total) {
+template <typename I>
+__device__ I block_exclusive_scan(I v, long long* red, I* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  long long inc = v;
+  I inc = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long n = __shfl_up_sync(0xffffffffu, inc, o);
+    const I n = __shfl_up_sync(0xffffffffu, inc, o);
     if (lane >= o) inc += n;
   }
   __syncthreads();
   if (lane == 31) red[warp] = inc;
   __syncthreads();
-  long long before = 0, all = 0;
+  I before = 0, all = 0;
   for (int w = 0; w < kThreads / 32; ++w) {
-    const long long s = red[w];
+    const I s = static_cast<I>(red[w]);
     if (w < warp) before += s;
     all += s;
   }
@@ -88,21 +89,119 @@ __device__ long long block_exclusive_scan(long long v, long long* red, long long
 
 // Cuts of the row occupying groups [a, a + g) of the sequence: multiples of
 // W strictly inside, none within W / 8 of either end. Returns their number
-// and the first one.
+// and the first one. I is int when the whole sequence fits (the usual case:
+// 32-bit division is far cheaper), else long long.
+template <typename I>
 struct Cuts {
-  long long first;
+  I first;
   int count;
 };
 
-__device__ __forceinline__ Cuts row_cuts(long long a, int g, long long W) {
-  const long long d = W / 8;
-  const long long lo = a + d + 1, hi = a + g - d - 1;  // allowed cut positions
-  Cuts c{0, 0};
+template <typename I>
+__device__ __forceinline__ Cuts<I> row_cuts(I a, int g, I W) {
+  const I d = W / 8;
+  const I lo = a + d + 1, hi = a + g - d - 1;  // allowed cut positions
+  Cuts<I> c{0, 0};
   if (g > 0 && hi >= lo) {
     c.first = (lo + W - 1) / W * W;
     if (c.first <= hi) c.count = static_cast<int>((hi - c.first) / W + 1);
   }
   return c;
+}
+
+// The histogram, the ranking and the items, with positions of type I.
+template <typename I, typename Info>
+__device__ void schedule_items(const SchedParams& p, Info info, I W, long long* red, int* hist, int* start) {
+  const int tid = threadIdx.x;
+  const int U = p.num_units;
+  // piece-size histogram; rows of unit u start at pos_u (unit-major)
+  for (int b = tid; b < kSizeBins; b += kThreads) hist[b] = 0;
+  I carry = 0;
+  for (int u0 = 0; u0 < U; u0 += kThreads) {
+    const int u = u0 + tid;
+    UnitInfo i{0, 0};
+    if (u < U) i = info(u);
+    I sum;
+    const I pos = carry + block_exclusive_scan<I>(static_cast<I>(i.tiles) * i.groups, red, &sum);
+    carry += sum;
+    for (int t = 0; t < i.tiles; ++t) {
+      const I a = pos + static_cast<I>(t) * i.groups;
+      const Cuts<I> c = row_cuts<I>(a, i.groups, W);
+      I prev = a;
+      for (int j = 0; j <= c.count; ++j) {
+        const I next = j < c.count ? c.first + j * W : a + i.groups;
+        atomicAdd(&hist[static_cast<int>(min(static_cast<long long>(next - prev),
+                                             static_cast<long long>(kSizeBins - 1)))], 1);
+        prev = next;
+      }
+    }
+  }
+  __syncthreads();
+  // start[b] = number of pieces in bins above b (kBinsPer bins per thread,
+  // thread 0 taking the largest)
+  {
+    constexpr int kBinsPer = kSizeBins / kThreads;
+    const int top = kSizeBins - 1 - kBinsPer * tid;
+    int mine = 0;
+#pragma unroll
+    for (int j = 0; j < kBinsPer; ++j) mine += hist[top - j];
+    int all;
+    int before = block_exclusive_scan<int>(mine, red, &all);
+#pragma unroll
+    for (int j = 0; j < kBinsPer; ++j) {
+      start[top - j] = before;
+      before += hist[top - j];
+    }
+  }
+  __syncthreads();
+  for (int b = tid; b < kSizeBins; b += kThreads) hist[b] = 0;  // now the per-bin cursor
+  __syncthreads();
+
+  // items, unit table and partial slots (slots of split rows, row order)
+  carry = 0;
+  int slot_carry = 0;
+  long long n_items = 0;
+  for (int u0 = 0; u0 < U; u0 += kThreads) {
+    const int u = u0 + tid;
+    UnitInfo i{0, 0};
+    if (u < U) i = info(u);
+    I sum;
+    const I pos = carry + block_exclusive_scan<I>(static_cast<I>(i.tiles) * i.groups, red, &sum);
+    carry += sum;
+    int nslots = 0;
+    for (int t = 0; t < i.tiles; ++t) {
+      const Cuts<I> c = row_cuts<I>(pos + static_cast<I>(t) * i.groups, i.groups, W);
+      if (c.count > 0) nslots += c.count + 1;
+    }
+    int slot_sum;
+    int slot = slot_carry + block_exclusive_scan<int>(nslots, red, &slot_sum);
+    slot_carry += slot_sum;
+    for (int t = 0; t < i.tiles; ++t) {
+      const I a = pos + static_cast<I>(t) * i.groups;
+      const Cuts<I> c = row_cuts<I>(a, i.groups, W);
+      const int k = c.count + 1;
+      const int pbase = k > 1 ? slot : -1;
+      reinterpret_cast<int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + t] = make_int2(pbase, k);
+      I prev = a;
+      for (int j = 0; j < k; ++j) {
+        const I next = j < c.count ? c.first + j * W : a + i.groups;
+        const int bin = static_cast<int>(min(static_cast<long long>(next - prev),
+                                             static_cast<long long>(kSizeBins - 1)));
+        const int at = start[bin] + atomicAdd(&hist[bin], 1);
+        int4* it = reinterpret_cast<int4*>(p.items) + 2 * static_cast<int64_t>(at);
+        const long long kb = static_cast<long long>(prev - a) * kGroupKeys;
+        const long long ke = static_cast<long long>(next - a) * kGroupKeys;
+        it[0] = make_int4(u, t, static_cast<int>(min(kb, static_cast<long long>(INT32_MAX))),
+                          static_cast<int>(min(ke, static_cast<long long>(INT32_MAX))));
+        it[1] = make_int4(k > 1 ? pbase + j : -1, 0, 0, 0);
+        prev = next;
+      }
+      n_items += k;
+      if (k > 1) slot += k;
+    }
+  }
+  n_items = block_sum(n_items, red);
+  if (tid == 0) *p.n_items = static_cast<int32_t>(n_items);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams p) {
@@ -134,91 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams
   total = block_sum(total, red);  // (its barriers also publish the cache)
   const long long pairs = p.split_cap / 2 > 0 ? p.split_cap / 2 : 1;
   const long long W = total > 0 ? (total + pairs - 1) / pairs : 1;
-
-  // piece-size histogram; rows of unit u start at pos_u (unit-major)
-  for (int b = tid; b < kSizeBins; b += kThreads) hist[b] = 0;
-  long long carry = 0;
-  for (int u0 = 0; u0 < U; u0 += kThreads) {
-    const int u = u0 + tid;
-    UnitInfo i{0, 0};
-    if (u < U) i = info(u);
-    long long sum;
-    const long long pos = carry + block_exclusive_scan(static_cast<long long>(i.tiles) * i.groups, red, &sum);
-    carry += sum;
-    for (int t = 0; t < i.tiles; ++t) {
-      const long long a = pos + static_cast<long long>(t) * i.groups;
-      const Cuts c = row_cuts(a, i.groups, W);
-      long long prev = a;
-      for (int j = 0; j <= c.count; ++j) {
-        const long long next = j < c.count ? c.first + j * W : a + i.groups;
-        atomicAdd(&hist[static_cast<int>(min(next - prev, static_cast<long long>(kSizeBins - 1)))], 1);
-        prev = next;
-      }
-    }
-  }
-  __syncthreads();
-  // start[b] = number of pieces in bins above b (kBinsPer bins per thread,
-  // thread 0 taking the largest)
-  {
-    constexpr int kBinsPer = kSizeBins / kThreads;
-    const int top = kSizeBins - 1 - kBinsPer * tid;
-    int mine = 0;
-#pragma unroll
-    for (int j = 0; j < kBinsPer; ++j) mine += hist[top - j];
-    long long all;
-    int before = static_cast<int>(block_exclusive_scan(mine, red, &all));
-#pragma unroll
-    for (int j = 0; j < kBinsPer; ++j) {
-      start[top - j] = before;
-      before += hist[top - j];
-    }
-  }
-  __syncthreads();
-  for (int b = tid; b < kSizeBins; b += kThreads) hist[b] = 0;  // now the per-bin cursor
-  __syncthreads();
-
-  // items, unit table and partial slots (slots of split rows, row order)
-  carry = 0;
-  long long slot_carry = 0, n_items = 0;
-  for (int u0 = 0; u0 < U; u0 += kThreads) {
-    const int u = u0 + tid;
-    UnitInfo i{0, 0};
-    if (u < U) i = info(u);
-    long long sum;
-    const long long pos = carry + block_exclusive_scan(static_cast<long long>(i.tiles) * i.groups, red, &sum);
-    carry += sum;
-    int nslots = 0;
-    for (int t = 0; t < i.tiles; ++t) {
-      const Cuts c = row_cuts(pos + static_cast<long long>(t) * i.groups, i.groups, W);
-      if (c.count > 0) nslots += c.count + 1;
-    }
-    long long slot_sum;
-    int slot = static_cast<int>(slot_carry + block_exclusive_scan(nslots, red, &slot_sum));
-    slot_carry += slot_sum;
-    for (int t = 0; t < i.tiles; ++t) {
-      const long long a = pos + static_cast<long long>(t) * i.groups;
-      const Cuts c = row_cuts(a, i.groups, W);
-      const int k = c.count + 1;
-      const int pbase = k > 1 ? slot : -1;
-      reinterpret_cast<int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + t] = make_int2(pbase, k);
-      long long prev = a;
-      for (int j = 0; j < k; ++j) {
-        const long long next = j < c.count ? c.first + j * W : a + i.groups;
-        const int bin = static_cast<int>(min(next - prev, static_cast<long long>(kSizeBins - 1)));
-        const int at = start[bin] + atomicAdd(&hist[bin], 1);
-        int4* it = reinterpret_cast<int4*>(p.items) + 2 * static_cast<int64_t>(at);
-        const long long kb = (prev - a) * kGroupKeys, ke = (next - a) * kGroupKeys;
-        it[0] = make_int4(u, t, static_cast<int>(min(kb, static_cast<long long>(INT32_MAX))),
-                          static_cast<int>(min(ke, static_cast<long long>(INT32_MAX))));
-        it[1] = make_int4(k > 1 ? pbase + j : -1, 0, 0, 0);
-        prev = next;
-      }
-      n_items += k;
-      if (k > 1) slot += k;
-    }
-  }
-  n_items = block_sum(n_items, red);
-  if (tid == 0) *p.n_items = static_cast<int32_t>(n_items);
+  if (total < (1ll << 30))
+    schedule_items<int>(p, info, static_cast<int>(W), red, hist, start);
+  else
+    schedule_items<long long>(p, info, W, red, hist, start);
 }
 
 }  // namespace
