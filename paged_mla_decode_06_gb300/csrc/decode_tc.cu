@@ -1,8 +1,10 @@
 // decode_tc.cu -- split-K paged MLA decode on tcgen05 tensor cores (sm_103a).
 //
 // A CTA pair (thread-block cluster of 2) owns one (128-row tile, segment,
-// request). Rows are (token, head) pairs of the request; all of them share
-// one pass over each KV page. The pair splits the work by stage, so that the
+// request), or, under the balanced schedule, the work item its blockIdx
+// selects from the list the schedule kernel wrote (request, tile, key range,
+// partial slot). Rows are (token, head) pairs of the request; all of them
+// share one pass over each KV page. The pair splits the work by stage, so that the
 // only traffic between the two SMs is the probabilities:
 //   score CTA (rank 0) -- S_g = Q K_g^T over all 576 columns of a 128-key
 //       group (M=128, N=128, fp32 in TMEM, two buffers; kind::f16 with q's
@@ -20,10 +22,11 @@
 //       rescaled in TMEM before the product; the epilogue scales O by the
 //       per-row factor the score CTA sends at the end.
 // Warps: 0 TMA (q, block-table lookup, key boxes), 1 MMA issue, 2-5
-// softmax (score CTA) or O rescale + epilogue (value CTA), 6-9 row gather
-// (sparse), e4m3 -> f16 widening of the value columns (value CTA, e4m3) or
-// more TMA producers (6-8): one warp issuing TMA loads moves only ~27 bytes
-// per SM clock, several keep the SM's load path busy. The value CTA re-reads
+// softmax (score CTA) or O rescale + epilogue (value CTA), 6-9 sparse row
+// gathers (TMA gather4, four 128-byte rows per lane), e4m3 -> f16 widening
+// of the value columns (value CTA, e4m3) or more TMA producers (6-8): one
+// warp issuing TMA loads moves only ~27 bytes per SM clock, several keep the
+// SM's load path busy. The value CTA re-reads
 // the first 512 columns of each row, which the score CTA has just pulled
 // through L2.
 // Every wait is bounded; on a timeout the kernel records an error code in
