@@ -5,9 +5,13 @@
 A step is one full decode call (split-K segments + merge, through the C ABI)
 over one batch of the DeepSeek-V3-shaped bf16 workload: 64 requests, 128
 heads, qlen 1, seq_lens uniform in [1024, 8192], block 64, values ~N(0, 1),
-random page permutation, segments chosen by the planner. Inputs are seeded
-and synthetic. L2 is flushed (a 256 MiB write) before every timed step, and
-only the step itself is inside its CUDA events.
+random page permutation, segments chosen by the planner. With the planner's
+balanced schedule a call is three launches: the work list from the lengths,
+the decode over it, and the merge of the rows the list split. Inputs are
+seeded and synthetic. L2 is flushed (a 256 MiB write) before every timed
+step, and only the step itself is inside its CUDA events. The roofline's
+kernel time is the decode launch alone, timed the same way on the same work
+list.
 
 Under torchrun (N > 1) every rank decodes its own batch of the same shape
 (weak scaling, no collective on the data path); the per-step time is the max
