@@ -455,6 +455,35 @@ def test_side_stream_and_graph_replay(kernel):
                  "graph replay")
 
 
+def test_balanced_schedule_graph_replay():
+    """The balanced call (schedule, decode, merge; the last two programmatic
+    dependents of the launch before them) captured in a CUDA graph and
+    replayed with other lengths in the same device buffer: the work list is
+    rebuilt from the new lengths inside the graph."""
+    w = I.dsv3_bf16(batch=6, seq_lo=300, seq_hi=3000, num_segments=0)
+    dw = B.DeviceWorkload(w, kernel=B.MLA_KERNEL_TCGEN05)
+    assert dw.plan.schedule == 1
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        dw.forward()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        dw.forward()
+    w2 = I.dsv3_bf16(batch=6, seq_lo=300, seq_hi=3000, num_segments=0)
+    # shorter by different amounts (inside every request's blocks): another work list
+    w2.seq_lens = np.maximum(w.seq_lens - np.array([101, 900, 13, 500, 1700, 64]), 1).astype(np.int32)
+    dw.seq_lens.copy_(torch.from_numpy(w2.seq_lens))
+    dw.out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert dw.status() == 0
+    ro2, rl2 = run_oracle(w2)
+    assert_close(dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), ro2, rl2, "bf16",
+                 "balanced graph replay")
+
+
 # ---------------------------------------------------------------- full-size workloads
 
 def _sampled(w, tokens, ns=None):
