@@ -139,8 +139,9 @@ typedef struct {
  * tile_size = min(128, largest power of two dividing block_size)
  * ([dense] _segmented_mla_page_size); the sparse variant has no page
  * structure and uses a 64-entry tile.
- * Balanced schedule: when the tensor-core kernel runs and prob->num_segments
- * is 0, the plan sets schedule = 1 and num_segments = 1, and mla_decode_fwd
+ * Balanced schedule: when the tensor-core kernel runs, prob->num_segments
+ * is 0 and units x row tiles is at most 2^20 (else NS = 1 with the uniform
+ * partition), the plan sets schedule = 1 and num_segments = 1, and mla_decode_fwd
  * sizes the segments on the device from the lengths of the call (the work
  * list of [sparse] _forward_mla's persistent path, work_indptr /
  * reduce_indptr / reduce_partial_map). Rows (a unit, i.e. a dense request or
