@@ -19,27 +19,32 @@ namespace {
 constexpr int kSeqThreads = 1024;
 constexpr int kFitWarps = 4;
 
-// One block; tokens in chunks of 1024, a block-wide exclusive scan per chunk.
+// One block. Pass 1, one thread per request: the lengths of the request's
+// tokens go to indptr[t + 1] (scratch). Pass 2, tokens in chunks of 1024:
+// each thread reads its length (before any write of the chunk: the scan's
+// barriers separate them), then indptr[t] = the exclusive prefix.
 __global__ void __launch_bounds__(kSeqThreads, 1) sparse_seqlen_kernel(
     const int32_t* __restrict__ qsl, const int32_t* __restrict__ seq_lens, int32_t num_reqs,
     int32_t num_tokens, int32_t topk, int32_t* __restrict__ lens, int32_t* __restrict__ indptr) {
   __shared__ int warp_sum[kSeqThreads / 32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int r = tid; r < num_reqs; r += kSeqThreads) {
+    const int q0 = qsl[r], q1 = qsl[r + 1];
+    const int qlen = q1 - q0;
+    const int64_t base = static_cast<int64_t>(seq_lens[r]) - qlen + 1;
+    for (int j = 0; j < qlen; ++j) {
+      const int t = q0 + j;
+      if (t < 0 || t >= num_tokens) continue;
+      const int64_t visible = base + j;
+      indptr[t + 1] = static_cast<int>(visible < 0 ? 0 : (visible > topk ? topk : visible));
+    }
+  }
+  const int covered = num_reqs > 0 ? min(qsl[num_reqs], num_tokens) : 0;
+  __syncthreads();  // pass 1's global writes are visible to the whole block
   int carry = 0;
   for (int t0 = 0; t0 < num_tokens; t0 += kSeqThreads) {
     const int t = t0 + tid;
-    int len = 0;
-    if (t < num_tokens && num_reqs > 0 && t < qsl[num_reqs]) {
-      int lo = 0, hi = num_reqs - 1;  // last request r with qsl[r] <= t
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (qsl[mid] <= t) lo = mid; else hi = mid - 1;
-      }
-      const int qlen = qsl[lo + 1] - qsl[lo];
-      const int j = t - qsl[lo];
-      const int64_t visible = static_cast<int64_t>(seq_lens[lo]) - qlen + j + 1;
-      len = static_cast<int>(visible < 0 ? 0 : (visible > topk ? topk : visible));
-    }
+    const int len = t < covered ? indptr[t + 1] : 0;
     int inc = len;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
