@@ -8,6 +8,8 @@ import glob
 import os
 import re
 
+import numpy as np
+
 import pytest
 
 from paged_mla_decode_06_gb300 import binding as B
@@ -305,3 +307,57 @@ def test_fit_kpool_rejects_bad_arguments(lib):
     assert f(out=FAKE + 64) == B.MLA_ERR_INVALID_ARG  # overlaps the input rows
     assert f(ti=None) == B.MLA_ERR_INVALID_ARG
     assert f(T=0) == B.MLA_OK                         # nothing to launch
+
+
+def test_plan_random_problems_are_consistent(lib):
+    """Random valid problems: the plan succeeds and its launch shape and
+    workspace layout hold together; random invalid ones are refused."""
+    rng = np.random.default_rng(123)
+    for _ in range(400):
+        sparse = rng.random() < 0.3
+        heads = int(rng.integers(1, 129))
+        bs = int(rng.choice([1, 16, 48, 64, 128, 256]))
+        sms = int(rng.choice([2, 16, 100, 152]))
+        ns = int(rng.choice([0, 0, 1, 3, 16]))
+        if sparse:
+            T = int(rng.integers(1, 3000))
+            prob = B.make_problem(num_tokens=T, num_heads=heads, block_size=bs, num_blocks=1000,
+                                  topk=128 * int(rng.integers(1, 17)), num_segments=ns, num_sms=sms,
+                                  dtype="bf16")
+            units = T
+        else:
+            R = int(rng.integers(1, 2000))
+            qlen = int(rng.integers(1, 5))
+            mb = int(rng.integers(1, 300))
+            prob = B.make_problem(num_tokens=R * qlen, num_reqs=R, num_heads=heads, block_size=bs,
+                                  num_blocks=100000, max_blocks_per_req=mb,
+                                  max_seq_len=int(rng.integers(0, mb * bs + 1)), max_qlen=qlen,
+                                  num_segments=ns, num_sms=sms,
+                                  dtype=str(rng.choice(["bf16", "fp8"])))
+            units = R
+        plan = B.mla_decode_plan(prob)
+        assert plan.num_segments >= 1 and plan.tile_size >= 1 and plan.row_tiles >= 1
+        assert plan.grid_x >= 1 and plan.grid_y >= 1 and plan.grid_z == units
+        assert plan.workspace_bytes >= 256 and plan.workspace_bytes % 256 == 0
+        if plan.schedule == 1:
+            assert plan.kernel == 4 and ns == 0 and plan.num_segments == 1
+            pairs = max(1, sms // 2)
+            assert plan.split_items == 2 * pairs
+            assert plan.max_items == units * plan.row_tiles + pairs
+            rows = plan.split_items * 128
+            assert plan.segm_output_offset >= 512 + plan.max_items * 32
+            assert plan.segm_max_offset >= plan.segm_output_offset + rows * 512 * 4
+            assert plan.segm_expsum_offset >= plan.segm_max_offset + rows * 4
+            assert plan.workspace_bytes >= plan.segm_expsum_offset + rows * 4
+        elif plan.num_segments > 1:
+            th = prob.num_tokens * heads
+            assert plan.segm_max_offset >= plan.segm_output_offset + th * plan.num_segments * 512 * 4
+            assert plan.workspace_bytes >= plan.segm_expsum_offset + th * plan.num_segments * 4
+        # the same problem with one field broken is refused
+        bad = B.make_problem(num_tokens=prob.num_tokens, num_reqs=prob.num_reqs, num_heads=heads,
+                             block_size=bs, num_blocks=prob.num_blocks,
+                             max_blocks_per_req=prob.max_blocks_per_req, max_seq_len=prob.max_seq_len,
+                             max_qlen=prob.max_qlen, topk=prob.topk, num_sms=sms,
+                             num_segments=int(rng.choice([-1, 65])))
+        out = B.Plan()
+        assert lib.mla_decode_plan(ctypes.byref(bad), ctypes.byref(out)) == B.MLA_ERR_INVALID_ARG
