@@ -363,8 +363,8 @@ def run_gpu(args):
     for _ in range(args.warmup):
         dw.forward()
     barrier()
-    sampler = ClockSampler(dev.index or 0, os.path.join(ROOT, "gpurun_out", "clocks.csv")
-                           if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else None)
+    # the raw clock samples go to a CSV only when MLA_BENCH_CLOCKS_CSV names one
+    sampler = ClockSampler(dev.index or 0, os.environ.get("MLA_BENCH_CLOCKS_CSV") or None)
     sampler.start()
     barrier()
     t_wall = time.perf_counter()
