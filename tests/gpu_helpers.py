@@ -8,11 +8,20 @@ from paged_mla_decode_06_gb300 import binding as B
 
 TOL_OUT = {"bf16": 1e-2, "fp8": 2e-2}
 TOL_LSE = 1e-3
-# Rows that see only a handful of keys of unit-variance values lie outside
-# the specified workloads (whose outputs average hundreds of keys). There one
-# p rounded to bf16 (relative error <= 2^-9) moves the output by up to
-# 2^-9 * max|v|, and rounding the output to bf16 adds up to 2^-8 * |out|:
-# for |v|, |out| <= 4.5 that is 0.009 + 0.018 < 3e-2.
+# Per-row tolerance. A row's output is a softmax-weighted mean of its visible
+# values (unit-variance draws in these tests). With scores of variance s2 the
+# effective number of keys behind a row is about n * exp(-s2) (s2 = 3 for the
+# N(0, 1) workloads at scale 1/sqrt(192)), so a row of n >= FEW_KEYS = 256 keys
+# averages >= 12 values and |out| stays below ~1.5: rounding the output to
+# bf16 (unit roundoff 2^-8) costs at most 0.006 there, and the independent
+# roundings of its many probabilities to 16 bits average out far below that,
+# so such rows must meet the workload bounds TOL_OUT.
+# A row of fewer keys can be dominated by one or two values of magnitude up
+# to ~4.5: the output rounding alone then reaches 2^-8 * 4.5 = 0.018, and a
+# probability rounded to bf16 moves the output by up to another 2^-8 * 4.5
+# when only a couple of keys carry the weight; such rows are held to
+# TOL_FEW_KEYS = 3e-2.
+FEW_KEYS = 256
 TOL_FEW_KEYS = 3e-2
 
 
@@ -40,16 +49,56 @@ def run_oracle(w, tokens=None, slots=None):
                         qo_indptr=w.qo_indptr, sinks=w.sinks, tokens=tokens)
 
 
-def assert_close(out, lse, ref_out, ref_lse, dtype="bf16", what="", tol=None):
-    tol = TOL_OUT[dtype] if tol is None else tol
+def visible_keys(w, tokens=None, slots=None, indptr=None):
+    """Keys each token's rows see: the causal length of its request position
+    (dense), or its valid slots (sparse; ``slots`` [T, K] or a flat list with
+    ``indptr``, default the workload's own top-k rows). Counted here from the
+    inputs, with no decode arithmetic."""
+    T = w.num_tokens
+    n = np.zeros(T, dtype=np.int64)
+    if w.sparse or slots is not None:
+        if indptr is not None:
+            flat = np.asarray(slots)
+            for t in range(T):
+                n[t] = int((flat[indptr[t]:indptr[t + 1]] >= 0).sum())
+        else:
+            s = np.asarray(w.topk_indices if slots is None else slots)
+            n = (s >= 0).sum(axis=1).astype(np.int64)
+    elif w.qo_indptr is None:
+        n = w.seq_lens.astype(np.int64).copy()
+    else:
+        for r in range(w.num_reqs):
+            a, b = int(w.qo_indptr[r]), int(w.qo_indptr[r + 1])
+            for j in range(b - a):
+                n[a + j] = max(0, int(w.seq_lens[r]) - (b - a) + j + 1)
+    return n if tokens is None else n[np.asarray(tokens)]
+
+
+def assert_close(out, lse, ref_out, ref_lse, dtype="bf16", what="", keys=None):
+    """Element-wise comparison, tolerance per row: rows of tokens that see at
+    least FEW_KEYS keys (or every row when ``keys`` is None) are held to the
+    workload bound TOL_OUT[dtype]; rows of fewer keys to TOL_FEW_KEYS. LSE to
+    TOL_LSE everywhere. Returns the largest error over the strict rows."""
     assert out.shape == ref_out.shape, (out.shape, ref_out.shape)
     assert np.isfinite(out).all(), f"{what}: non-finite output"
-    err = float(np.max(np.abs(out - ref_out))) if out.size else 0.0
-    assert err <= tol, f"{what}: max |out - oracle| = {err:.3e} > {tol}"
+    T = out.shape[0]
+    if keys is None:
+        keys = np.full(T, np.iinfo(np.int64).max)
+    keys = np.asarray(keys)
+    assert keys.shape == (T,), (keys.shape, T)
+    row_err = np.abs(out - ref_out).reshape(T, -1).max(axis=1) if out.size else np.zeros(T)
+    strict = keys >= FEW_KEYS
+    tol = np.where(strict, TOL_OUT[dtype], TOL_FEW_KEYS)
+    bad = np.nonzero(row_err > tol)[0]
+    if bad.size:
+        worst = sorted(bad, key=lambda t: -row_err[t])[:5]
+        msg = ", ".join(f"token {t}: {row_err[t]:.3e} > {tol[t]:.0e} ({keys[t]} keys)"
+                        for t in worst)
+        raise AssertionError(f"{what}: max |out - oracle| per row: {msg}")
     ninf = np.isneginf(ref_lse)
     assert np.array_equal(np.isneginf(lse), ninf), f"{what}: -inf lse pattern differs"
     assert not np.isnan(lse).any(), f"{what}: NaN lse"
     if (~ninf).any():
         lerr = float(np.max(np.abs(lse[~ninf] - ref_lse[~ninf])))
         assert lerr <= TOL_LSE, f"{what}: max |lse - oracle| = {lerr:.3e} > {TOL_LSE}"
-    return err
+    return float(row_err[strict].max()) if strict.any() else 0.0
