@@ -99,13 +99,19 @@ typedef struct {
                                   run this problem) */
 } mla_problem_t;
 
-/* Decode kernel variants. */
+/* Decode kernel variants. MLA_KERNEL_AUTO takes MLA_KERNEL_TCGEN05_ROWS_N
+ * where it can run, else MLA_KERNEL_TCGEN05, else MLA_KERNEL_WARP_MMA. */
 typedef enum {
   MLA_KERNEL_AUTO = 0,
   MLA_KERNEL_WARP_MMA = 1,     /* warp-level MMA split-K kernel: every shape */
-  MLA_KERNEL_TCGEN05 = 2       /* tcgen05/TMEM CTA-pair kernel: dense bf16 or
-                                  e4m3 with block_size a multiple of 64, or
+  MLA_KERNEL_TCGEN05 = 2,      /* tcgen05/TMEM CTA-pair kernel, 128 query rows
+                                  per pair as the MMA M dimension: dense bf16
+                                  or e4m3 with block_size a multiple of 64, or
                                   sparse bf16 */
+  MLA_KERNEL_TCGEN05_ROWS_N = 3 /* tcgen05/TMEM kernel with the query rows as
+                                  the MMA N dimension, one CTA per 16..64 rows:
+                                  dense e4m3 with block_size a multiple of 64
+                                  and num_heads * max_qlen <= 64 */
 } mla_kernel_t;
 
 /* Filled by mla_decode_plan; pass it unchanged to mla_decode_fwd or
@@ -122,8 +128,10 @@ typedef struct {
   int32_t num_sms;
   int32_t schedule;            /* 1: balanced schedule (see mla_decode_plan), else 0 */
   int32_t max_items;           /* balanced: work items the decode grid holds */
-  int32_t split_items;         /* balanced: partial slots of 128 rows, two per
-                                  CTA pair (2 * (num_sms / 2)) */
+  int32_t split_items;         /* balanced: partial slots of rows_per_cta rows,
+                                  two per worker: 2 * (num_sms / 2) for the
+                                  CTA-pair kernel, 2 * num_sms for the
+                                  rows-as-N kernel */
   int32_t reserved;
   size_t workspace_bytes;      /* bytes mla_decode_fwd needs (>= 256) */
   size_t status_offset;        /* workspace layout, 256-B aligned pieces: a device */
@@ -139,24 +147,25 @@ typedef struct {
  * tile_size = min(128, largest power of two dividing block_size)
  * ([dense] _segmented_mla_page_size); the sparse variant has no page
  * structure and uses a 64-entry tile.
- * Balanced schedule: when the tensor-core kernel runs, prob->num_segments
+ * Balanced schedule: when a tensor-core kernel runs, prob->num_segments
  * is 0 and units x row tiles is at most 2^20 (else NS = 1 with the uniform
  * partition), the plan sets schedule = 1 and num_segments = 1, and mla_decode_fwd
  * sizes the segments on the device from the lengths of the call (the work
  * list of [sparse] _forward_mla's persistent path, work_indptr /
  * reduce_indptr / reduce_partial_map). Rows (a unit, i.e. a dense request or
- * a sparse token, times its 128-query-row tiles) of g = cdiv(len, 128) key
- * groups are laid end to end and the sequence of all groups is cut every
- * W = cdiv(total, num_sms / 2) groups, cuts within W / 8 of a row's ends
- * dropped; the pieces run longest first (max_items = rows + num_sms / 2).
- * Unsplit rows are written by the decode kernel itself; split rows write
- * base-2 partials to 128-row slots of the workspace (split_items =
- * 2 * (num_sms / 2) of them) and mla_merge_items combines them. Workspace
- * layout: status block, item count at 256, items (32 bytes each, max_items
- * of them) at 512, the unit table (int32 pairs {first slot or -1, pieces}
- * per unit and row tile) at the next 256-byte boundary, then segm_output
- * [split_items * 128, 512], segm_max and segm_expsum [split_items * 128] at
- * the plan's offsets.
+ * a sparse token, times its tiles of rows_per_cta query rows) of
+ * g = cdiv(len, 128) key groups are laid end to end and the sequence of all
+ * groups is cut every W = cdiv(total, workers) groups (workers: num_sms / 2
+ * CTA pairs, or num_sms CTAs for the rows-as-N kernel), cuts within W / 8 of
+ * a row's ends dropped; the pieces run longest first (max_items = rows +
+ * workers). Unsplit rows are written by the decode kernel itself; split rows
+ * write base-2 partials to slots of rows_per_cta rows in the workspace
+ * (split_items = 2 * workers of them) and mla_merge_items combines them.
+ * Workspace layout: status block, item count at 256, items (32 bytes each,
+ * max_items of them) at 512, the unit table (int32 pairs {first slot or -1,
+ * pieces} per unit and row tile) at the next 256-byte boundary, then
+ * segm_output [split_items * rows_per_cta, 512], segm_max and segm_expsum
+ * [split_items * rows_per_cta] at the plan's offsets.
  * Errors: MLA_ERR_INVALID_ARG for NULL pointers or inconsistent sizes,
  * MLA_ERR_UNSUPPORTED for head_dim != 576, kv_lora_rank != 512,
  * num_heads > 128, q_dtype != kv_dtype, or topk not a multiple of 128.

@@ -25,6 +25,7 @@ MLA_DTYPE_FP8_E4M3 = 1
 MLA_KERNEL_AUTO = 0
 MLA_KERNEL_WARP_MMA = 1
 MLA_KERNEL_TCGEN05 = 2
+MLA_KERNEL_TCGEN05_ROWS_N = 3
 
 HEAD_DIM = 576
 KV_LORA_RANK = 512

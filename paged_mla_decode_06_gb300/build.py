@@ -20,8 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libmla_decode.so")
 
-SOURCES = ["api.cu", "decode_mma.cu", "decode_tc.cu", "merge.cu", "index_convert.cu", "sched.cu",
-           "q_prep.cu", "sparse_front.cu"]
+SOURCES = ["api.cu", "decode_mma.cu", "decode_tc.cu", "decode_hn.cu", "merge.cu", "index_convert.cu",
+           "sched.cu", "q_prep.cu", "sparse_front.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr",

@@ -48,7 +48,7 @@ mla_status_t check_problem(const mla_problem_t& p) {
   if (p.num_segments < 0 || p.num_segments > kMaxSegments) return MLA_ERR_INVALID_ARG;
   if (p.num_sms < 0 || p.has_sinks < 0 || p.has_sinks > 1) return MLA_ERR_INVALID_ARG;
   if (p.topk < 0) return MLA_ERR_INVALID_ARG;
-  if (p.kernel < MLA_KERNEL_AUTO || p.kernel > MLA_KERNEL_TCGEN05) return MLA_ERR_INVALID_ARG;
+  if (p.kernel < MLA_KERNEL_AUTO || p.kernel > MLA_KERNEL_TCGEN05_ROWS_N) return MLA_ERR_INVALID_ARG;
   if (p.topk > 0) {
     if (p.topk % 128 != 0) return MLA_ERR_UNSUPPORTED;
     if (p.max_qlen > 1) return MLA_ERR_INVALID_ARG;  // sparse rows are single tokens
@@ -169,18 +169,23 @@ SchedLayout sched_layout(const mla_plan_t* plan) {
   return l;
 }
 
-// d.items selects the balanced grid: one CTA pair per item slot.
+// d.items selects the balanced grid: one CTA pair (or CTA) per item slot.
 mla_status_t launch_decode(const mla_plan_t* plan, const mla::DecodeParams& d, int* status,
                            cudaStream_t stream) {
   if (plan->grid_z == 0) return MLA_OK;
   const mla_problem_t& p = plan->prob;
+  const int64_t q_rows = static_cast<int64_t>(p.num_tokens) * p.num_heads;
+  const int64_t kv_rows = static_cast<int64_t>(p.num_blocks) * p.block_size;
+  const unsigned items = static_cast<unsigned>(plan->max_items);
   if (plan->kernel == mla::kTcPair128) {
-    const int64_t q_rows = static_cast<int64_t>(p.num_tokens) * p.num_heads;
-    const int64_t kv_rows = static_cast<int64_t>(p.num_blocks) * p.block_size;
-    const dim3 grid = d.items != nullptr ? dim3(2u * static_cast<unsigned>(plan->max_items), 1u, 1u)
-                                         : grid_of(plan);
+    const dim3 grid = d.items != nullptr ? dim3(2u * items, 1u, 1u) : grid_of(plan);
     return cuda_status(mla::launch_decode_tc(d, p.kv_dtype == MLA_DTYPE_FP8_E4M3, q_rows, kv_rows,
                                              grid, status, stream));
+  }
+  if (plan->kernel == mla::kTcRowsN) {
+    const dim3 grid = d.items != nullptr ? dim3(items, 1u, 1u) : grid_of(plan);
+    return cuda_status(mla::launch_decode_hn(d, plan->rows_per_cta, q_rows, kv_rows, grid, status,
+                                             stream));
   }
   return cuda_status(mla::launch_decode_mma(plan->kernel, p.kv_dtype == MLA_DTYPE_FP8_E4M3, d,
                                             grid_of(plan), stream));
@@ -200,6 +205,7 @@ mla::SchedParams sched_params(const mla_plan_t* plan, const Inputs& in, uint8_t*
   sp.num_units = p.topk > 0 ? p.num_tokens : p.num_reqs;
   sp.num_heads = p.num_heads;
   sp.tiles_max = plan->row_tiles;
+  sp.tile_rows = plan->rows_per_cta;
   sp.split_cap = plan->split_items;
   sp.items = reinterpret_cast<int32_t*>(ws + l.items);
   sp.n_items = reinterpret_cast<int32_t*>(ws + l.n_items);
@@ -209,8 +215,8 @@ mla::SchedParams sched_params(const mla_plan_t* plan, const Inputs& in, uint8_t*
 
 mla_status_t check_scheduled(const mla_plan_t* plan, const void* workspace, size_t workspace_bytes) {
   if (plan == nullptr || plan->schedule != 1) return MLA_ERR_INVALID_ARG;
-  if (plan->kernel != mla::kTcPair128 || plan->max_items <= 0 || plan->split_items <= 0 ||
-      plan->row_tiles <= 0)
+  if ((plan->kernel != mla::kTcPair128 && plan->kernel != mla::kTcRowsN) || plan->max_items <= 0 ||
+      plan->split_items <= 0 || plan->row_tiles <= 0 || plan->rows_per_cta <= 0)
     return MLA_ERR_INVALID_ARG;
   if (workspace == nullptr || workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE;
   if (!aligned(workspace, kWsAlign)) return MLA_ERR_INVALID_ARG;
@@ -256,6 +262,7 @@ mla_status_t run_merge_items(const mla_plan_t* plan, const Inputs& in, const flo
   m.lse = lse;
   m.unit_tab = sp.unit_tab;
   m.tiles_max = plan->row_tiles;
+  m.tile_rows = plan->rows_per_cta;
   m.sparse = sp.sparse;
   return cuda_status(mla::launch_merge(m, stream));
 }
@@ -299,11 +306,21 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   const bool sparse = p.topk > 0;
   const int32_t units = sparse ? p.num_tokens : p.num_reqs;
   const int64_t rows_per_unit = sparse ? p.num_heads : static_cast<int64_t>(p.num_heads) * p.max_qlen;
+  // the CTA-pair kernel: 128-row tiles, dense (block size a multiple of 64) or sparse bf16;
+  // the rows-as-N kernel: e4m3 dense (block size a multiple of 64), at most 64 rows
   const bool tc_ok = sparse ? p.kv_dtype == MLA_DTYPE_BF16 : p.block_size % 64 == 0;
+  const bool rn_ok = !sparse && p.kv_dtype == MLA_DTYPE_FP8_E4M3 && p.block_size % 64 == 0 &&
+                     rows_per_unit <= 64;
   if (p.kernel == MLA_KERNEL_TCGEN05 && !tc_ok) return MLA_ERR_UNSUPPORTED;
-  const bool use_tc = tc_ok && p.kernel != MLA_KERNEL_WARP_MMA;
+  if (p.kernel == MLA_KERNEL_TCGEN05_ROWS_N && !rn_ok) return MLA_ERR_UNSUPPORTED;
+  const bool use_rn = p.kernel == MLA_KERNEL_TCGEN05_ROWS_N || (p.kernel == MLA_KERNEL_AUTO && rn_ok);
+  const bool use_pair = !use_rn && tc_ok && p.kernel != MLA_KERNEL_WARP_MMA;
+  const bool use_tc = use_rn || use_pair;
   int32_t kernel, rows;
-  if (use_tc) {
+  if (use_rn) {
+    kernel = mla::kTcRowsN;
+    rows = static_cast<int32_t>((rows_per_unit + 15) / 16 * 16);
+  } else if (use_pair) {
     kernel = mla::kTcPair128;
     rows = 128;
   } else if (rows_per_unit <= 16) {
@@ -344,18 +361,20 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   plan->kernel = kernel;
   plan->rows_per_cta = rows;
   plan->row_tiles = row_tiles;
-  plan->grid_x = use_tc ? 2 * row_tiles : row_tiles;  // a CTA pair per row tile
+  plan->grid_x = use_pair ? 2 * row_tiles : row_tiles;  // a CTA pair per row tile
   plan->grid_y = ns;
   plan->grid_z = units;
   plan->status_offset = 0;
   plan->workspace_bytes = kWsAlign;
   if (balanced) {
-    const int32_t split_cap = 2 * (sms / 2 > 0 ? sms / 2 : 1);
+    // workers: CTA pairs of the 128-row kernel, CTAs of the rows-as-N kernel
+    const int32_t workers = use_pair ? (sms / 2 > 0 ? sms / 2 : 1) : (sms > 0 ? sms : 1);
+    const int32_t split_cap = 2 * workers;
     plan->schedule = 1;
     plan->split_items = split_cap;
-    plan->max_items = static_cast<int32_t>(unit_tiles + split_cap / 2);  // rows + cuts
+    plan->max_items = static_cast<int32_t>(unit_tiles + workers);  // rows + cuts
     const SchedLayout l = sched_layout(plan);
-    const size_t slot_rows = static_cast<size_t>(split_cap) * 128;
+    const size_t slot_rows = static_cast<size_t>(split_cap) * rows;
     const size_t out_b = align_up(slot_rows * kRank * sizeof(float), kWsAlign);
     const size_t max_b = align_up(slot_rows * sizeof(float), kWsAlign);
     plan->segm_output_offset = l.end;

@@ -1,0 +1,810 @@
+// decode_hn.cu -- split-K paged MLA decode on tcgen05 tensor cores with the
+// query rows as the MMA N dimension (sm_103a): requests of at most 64 query
+// rows (heads x tokens) over an e4m3 cache whose block size is a multiple
+// of 64.
+//
+// A request of 16 heads padded to the 128-row M tile of the CTA-pair kernel
+// spends 7/8 of every QK^T, softmax and P.V step on padding. Here one CTA owns
+// one (tile of NR <= 64 rows, key range, request) and the operands swap roles,
+// per chunk of 128 keys:
+//   S^T[keys, rows]  = K Q^T   M = 128 keys, N = NR, K = 576: 18 kind::f8f6f4
+//                              instructions, A = the chunk's key rows (K-major,
+//                              straight from the TMA ring), B = q;
+//   O^T[cols, rows] += V^T P^T M = 128 value columns (four blocks of the 512),
+//                              N = the rows, K = the 128 keys: A = the same key
+//                              rows read MN-major, B = P^T, written by the
+//                              softmax threads one key per thread (MN-major,
+//                              8-key x 16-byte core matrices).
+// P goes to the tensor core as two e4m3 terms, hi = e4m3(p) and
+// lo = e4m3(p - hi), carrying ~8 significant bits of p (hi alone keeps 4,
+// which would move rows of a few keys by several hundredths); both terms are
+// one instruction of N = 2 NR (NR <= 48) or two of N = NR into the same
+// accumulator. A tcgen05 instruction with N <= 64 costs about as much as one
+// with N = 96 (measured), so the chunk costs ~34 instructions whatever NR is,
+// well inside the time its 72 KB take to arrive from HBM.
+// Softmax: a thread owns one key (a TMEM lane of S^T) and half of the rows (a
+// column each). A row's maximum over the chunk is a warp reduction
+// (redux.sync.max.f32) and an exchange among the softmax warps through
+// shared memory; p = 2^(s - m_ref + 4) with a reference max m_ref that moves
+// only when a chunk max exceeds it by more than 4 (O^T is then rescaled in
+// TMEM), so p <= 2^8 fits e4m3 and the bulk of the weights stays in its
+// normal range; the true max is kept for the partials.
+// Warps: 0, 2, 3 TMA producers (q; the key boxes through the block table), 1
+// MMA issue, 4-11 softmax and epilogue (a lane quarter of keys and half of
+// the rows each, two warps per SM sub-partition). Every wait is bounded: a timeout
+// records a code in the status word, stops the CTA's work, drains what it
+// issued and exits.
+#include <cfloat>
+#include <climits>
+
+#include "common.cuh"
+#include "internal.h"
+#include "tc_ops.cuh"
+#include "tma_map.cuh"
+
+namespace mla {
+namespace {
+
+using namespace tc;
+
+constexpr int kKeys = 128;               // keys per chunk: M of QK^T, K of P.V
+constexpr int kHalf = 64;                // keys per TMA box (rows of one block)
+constexpr int kSlot = kKeys * 128;       // ring slot: one 128-byte column box of a chunk
+constexpr int kBoxes = 5;                // per chunk: 4 latent boxes (512 e4m3) + the rope box
+constexpr int kThreads = 384;
+constexpr int kProducers = 3;            // warps 0, 2, 3
+constexpr int kSoftWarps = 8;            // warps 4-11: four TMEM lane quarters x two row halves
+constexpr int kMaxSlots = 14;
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+constexpr float kPBias = 4.f;            // p = 2^(s - m_ref + kPBias) <= 2^(2 kPBias)
+constexpr float kMove = 4.f;             // m_ref moves when a chunk max exceeds it by more
+
+enum : int {
+  kFull = 0,                    // [kMaxSlots] ring slot loaded
+  kEmpty = kMaxSlots,           // [kMaxSlots] ring slot free
+  kQFull = 2 * kMaxSlots,
+  kSFull,                       // [2] S^T buffer written
+  kSFree = kSFull + 2,          // [2] S^T buffer read
+  kPFull = kSFree + 2,          // [2] P^T buffer written
+  kPFree = kPFull + 2,          // [2] P.V of the buffer's chunk complete
+  kXA = kPFree + 2,             // [2] softmax warps: chunk maxima posted
+  kXB = kXA + 2,                // [2] softmax warps: reference maxima moved
+  kXE = kXB + 2,                // epilogue: row sums posted
+  kXF = kXE + 1,                // epilogue: row factors posted
+  kOFull = kXF + 1,             // last P.V complete
+  kDrain = kOFull + 1,
+  kNumBars = kDrain + 1
+};
+
+// Shared-memory header: barriers, TMEM address, abort flag, exchange arrays.
+constexpr int kOffBar = 0;
+constexpr int kOffTslot = 512;
+constexpr int kOffAbort = 516;
+constexpr int kOffIssued = 576;             // [kMaxSlots + 1] int: last use issued per ring slot, q
+constexpr int kOffWmax = 1024;              // [2][4][64] warp maxima of a chunk
+constexpr int kOffMref = kOffWmax + 2048;   // [64] reference max per row
+constexpr int kOffMtrue = kOffMref + 256;   // [64] true max per row
+constexpr int kOffAlpha = kOffMtrue + 256;  // [2][64] rescale factor per row
+constexpr int kOffResc = kOffAlpha + 512;   // [2] int: some row moved its reference
+constexpr int kOffVis = kOffResc + 256;     // [64] int: causal end of each row
+constexpr int kOffLsum = kOffVis + 256;     // [4][64] row sums per warp
+constexpr int kOffMult = kOffLsum + 1024;   // [64] output factor per row
+constexpr int kHeader = 6144;
+static_assert(kNumBars * 8 <= kOffTslot, "barrier space");
+static_assert(kOffIssued + 4 * (kMaxSlots + 1) <= 1024, "issue record space");
+static_assert(kOffMult + 256 <= kHeader, "header space");
+
+constexpr int align1k(int v) { return (v + 1023) / 1024 * 1024; }
+
+template <int NR>
+struct HnCfg {
+  static_assert(NR % 16 == 0 && NR >= 16 && NR <= 64, "16..64 rows in steps of 16");
+  static constexpr bool kConcat = NR <= 48;         // hi and lo as one MMA of N = 2 NR
+  static constexpr int kNpv = kConcat ? 2 * NR : NR;
+  static constexpr int kOCols = 4 * kNpv;           // O^T: 4 blocks of kNpv columns
+  static constexpr int kSCol = kOCols;              // S^T: 2 buffers of NR columns
+  static constexpr int kCols = kOCols + 2 * NR;
+  static constexpr uint32_t kTmemAlloc = kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128
+                                       : kCols <= 256 ? 256 : 512;
+  static_assert(kCols <= 512, "TMEM columns");
+  static constexpr int kQBox = NR * 128;            // one 128-byte column box of q
+  static constexpr int kOffQ = kHeader;
+  static constexpr int kPLbo = 16 * NR;             // P^T bytes per 8-key group (hi + lo cores)
+  static constexpr int kPBytes = kKeys * 2 * NR;    // one P^T buffer
+  // two P^T buffers (the softmax of chunk c + 1 writes while P.V of chunk c
+  // reads), one at 64 rows, where a second would cost the ring its tenth slot
+  static constexpr int kPBufs = NR == 64 ? 1 : 2;
+  static constexpr int kOffP = kOffQ + kBoxes * kQBox;
+  static constexpr int kOffRing = align1k(kOffP + kPBufs * kPBytes);
+  static constexpr int kUsable = 232448 - 1024;     // dynamic shared memory minus alignment slack
+  static constexpr int kSlotsFit = (kUsable - kOffRing) / kSlot;
+  static constexpr int kSlots = kSlotsFit < kMaxSlots ? kSlotsFit : kMaxSlots;
+  static constexpr int kSmem = kOffRing + kSlots * kSlot + 1024;
+  // QK^T of chunk c + 1 is issued before P.V of chunk c, which holds the
+  // ring indices of chunk c's value boxes: both chunks must fit the ring
+  static_assert(kSlots >= 2 * kBoxes, "ring slots");
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+struct HnMaps {
+  CUtensorMap q;   // q viewed as [T*H rows, 576] e4m3, box 128 bytes x NR rows
+  CUtensorMap kv;  // cache viewed as [NB*BS rows, 576] e4m3, box 128 bytes x 64 rows
+};
+
+struct Ctx {
+  uint8_t* smem;
+  uint32_t bar0;
+  volatile int* abort;
+  int* status;
+  uint64_t limit_ns;
+  uint32_t tbase;
+  int tid, warp, lane;
+  int H, tok0, qlen, row0, rows_total, part_len;
+  int seg, seg_start, seg_end, n_chunks, unit, pslot;
+  bool fin;
+  __device__ uint32_t bar(int i) const { return bar0 + 8u * i; }
+};
+
+__device__ __forceinline__ void report(int* status, int code) {
+  if (status != nullptr) atomicCAS(status, 0, code);
+}
+
+// Bounded wait on a barrier phase; false on timeout (recorded) or abort.
+__device__ bool wait_phase(const Ctx& x, uint32_t bar, uint32_t parity, int code) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*x.abort) return false;
+    if ((it & 15u) == 0) {
+      const uint64_t now = global_timer_ns();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > x.limit_ns) {
+        report(x.status, code);
+        *x.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// Every lane waits (each acquires what the phase published); warp-uniform result.
+__device__ __forceinline__ bool warp_wait(const Ctx& x, uint32_t bar, uint32_t parity, int code) {
+  return __all_sync(0xffffffffu, wait_phase(x, bar, parity, code)) != 0;
+}
+
+// Wait that ignores the abort flag (teardown drains), bounded by the default limit.
+__device__ void drain_wait(const Ctx& x, uint32_t bar, uint32_t parity, int code) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kDefaultWaitNs) {
+      report(x.status, code);
+      return;
+    }
+  }
+}
+
+// The softmax warps meet at barrier `idx` (one arrival per warp and phase):
+// this warp's shared-memory writes are published, the others' acquired.
+__device__ __forceinline__ bool cross_sync(const Ctx& x, int idx, uint32_t parity, int code) {
+  __syncwarp();
+  if (x.lane == 0) mbar_arrive(x.bar(idx));
+  return warp_wait(x, x.bar(idx), parity, code);
+}
+
+// Cache row of key position pos (64 keys from a 64-aligned position lie in
+// one block: the block size is a multiple of 64).
+__device__ __forceinline__ int cache_row(const DecodeParams& p, const int32_t* bt_row, int pos) {
+  const int bs = p.block_size;
+  const int blk = pos / bs;
+  return bt_row[blk] * bs + (pos - blk * bs);
+}
+
+// ------------------------------------------------------------------ producers
+// q (warp 0), then box j of chunk c (two 64-row TMA boxes from their
+// blocks) into ring slot i % kSlots, i = c * 5 + j, the boxes dealt
+// round-robin to the producer warps, which record the latest use issued per
+// slot (the teardown waits for those loads). The whole warp looks up the cache rows
+// of 16 chunks at a time (lane l: chunk l / 2, half l % 2), one window ahead
+// of the chunks it issues, so that no TMA issue waits on a block-table read;
+// lane 0 issues.
+template <int NR>
+__device__ void produce(const Ctx& x, const HnMaps& maps, const DecodeParams& p, int pidx) {
+  using C = HnCfg<NR>;
+  if (x.n_chunks == 0) return;
+  const int lane = x.lane;
+  volatile int* issued = reinterpret_cast<volatile int*>(x.smem + kOffIssued);
+  if (lane == 0) {
+    tma_prefetch_desc(&maps.kv);
+    if (pidx == 0) {
+      tma_prefetch_desc(&maps.q);
+      const int qrow = x.tok0 * x.H + x.row0;
+      issued[kMaxSlots] = 0;
+      mbar_arrive_expect_tx(x.bar(kQFull), kBoxes * C::kQBox);
+      for (int j = 0; j < kBoxes; ++j)
+        tma_load_2d(smem_u32(x.smem + C::kOffQ + j * C::kQBox), &maps.q, 128 * j, qrow, x.bar(kQFull));
+    }
+  }
+  const int32_t* bt_row = p.block_table + static_cast<int64_t>(x.unit) * p.bt_stride;
+  auto lookup = [&](int w0) {  // cache row of this lane's (chunk, half) in the window at w0
+    const int pos = x.seg_start + (w0 + (lane >> 1)) * kKeys + (lane & 1) * kHalf;
+    return pos < x.seg_end ? cache_row(p, bt_row, pos) : 0;
+  };
+  int cur = lookup(0);
+  int nxt = lookup(16);
+  const uint64_t pol = l2_evict_first();  // each key row is read once
+  int i = 0;
+  bool ok = true;
+  for (int c = 0; c < x.n_chunks && ok; ++c) {
+    if (c > 0 && (c & 15) == 0) {
+      cur = nxt;
+      nxt = lookup(c + 16);
+    }
+    const int row0 = __shfl_sync(0xffffffffu, cur, 2 * (c & 15));
+    const int row1 = __shfl_sync(0xffffffffu, cur, 2 * (c & 15) + 1);
+    const bool two = x.seg_start + c * kKeys + kHalf < x.seg_end;
+    if (lane == 0) {
+      for (int j = 0; j < kBoxes; ++j) {
+        const int ii = i + j;
+        if (ii % kProducers != pidx) continue;
+        const int slot = ii % C::kSlots;
+        const int use = ii / C::kSlots;
+        if (use >= 1 && !wait_phase(x, x.bar(kEmpty + slot), (use - 1) & 1, 11)) {
+          ok = false;
+          break;
+        }
+        const uint32_t dst = smem_u32(x.smem + C::kOffRing + slot * kSlot);
+        mbar_arrive_expect_tx(x.bar(kFull + slot), two ? kSlot : kSlot / 2);
+        tma_load_2d_hint(dst, &maps.kv, 128 * j, row0, x.bar(kFull + slot), pol);
+        if (two) tma_load_2d_hint(dst + kSlot / 2, &maps.kv, 128 * j, row1, x.bar(kFull + slot), pol);
+        atomicMax(const_cast<int*>(issued + slot), use);
+      }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    i += kBoxes;
+  }
+  __syncwarp();
+}
+
+// ------------------------------------------------------------------ MMA issue
+// Software-pipelined: S^T of chunk g, then O^T += V^T P^T of chunk g - 1, so
+// that the softmax of a chunk overlaps the QK^T of the next.
+template <int NR>
+__device__ void mma_issue(const Ctx& x) {
+  using C = HnCfg<NR>;
+  if (x.lane != 0) return;
+  constexpr uint32_t kIdQK = instr_desc(128, NR, 0, 0, false, false);
+  constexpr uint32_t kIdPV = instr_desc(128, C::kNpv, 0, 0, true, true);
+  const uint64_t q_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffQ), 16, 1024);
+  const uint64_t k_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffRing), 16, 1024);      // K-major
+  const uint64_t v_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffRing), kSlot, 1024);   // MN-major
+  const uint64_t p_desc = smem_desc_interleave(smem_u32(x.smem + C::kOffP), C::kPLbo, 128);
+  bool ok = x.n_chunks == 0 || wait_phase(x, x.bar(kQFull), 0, 21);
+  for (int g = 0; g <= x.n_chunks && ok; ++g) {
+    if (g < x.n_chunks) {
+      const int b = g & 1;
+      if (g >= 2 && !wait_phase(x, x.bar(kSFree + b), ((g - 2) >> 1) & 1, 22)) {
+        ok = false;
+        break;
+      }
+      const uint32_t d = x.tbase + C::kSCol + b * NR;
+#pragma unroll
+      for (int j = 0; j < kBoxes; ++j) {
+        const int i = g * kBoxes + j;
+        const int slot = i % C::kSlots;
+        if (!wait_phase(x, x.bar(kFull + slot), (i / C::kSlots) & 1, 23)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const uint64_t a = k_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
+        const uint64_t qb = q_desc + static_cast<uint64_t>(j * (C::kQBox >> 4));
+        // 32 e4m3 columns per instruction: 4 per latent box, 2 for the 64 rope columns
+#pragma unroll
+        for (int s = 0; s < (j < 4 ? 4 : 2); ++s)
+          mma_ss_f8(d, a + 2 * s, qb + 2 * s, kIdQK, (j | s) != 0 ? 1u : 0u);
+        if (j == 4) mma_commit(x.bar(kEmpty + slot));  // the rope box's only read
+      }
+      if (!ok) break;
+      mma_commit(x.bar(kSFull + b));
+    }
+    if (g >= 1) {
+      const int c = g - 1;
+      const int b = c & 1;
+      if (!wait_phase(x, x.bar(kPFull + b), (c >> 1) & 1, 24)) {
+        ok = false;
+        break;
+      }
+      fence_after_sync();
+      const uint64_t pb = p_desc + static_cast<uint64_t>((b % C::kPBufs) * (C::kPBytes >> 4));
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int slot = (c * kBoxes + m) % C::kSlots;
+        const uint64_t a = v_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
+        const uint32_t d = x.tbase + m * C::kNpv;
+#pragma unroll
+        for (int ks = 0; ks < kKeys / 32; ++ks) {
+          const uint64_t av = a + static_cast<uint64_t>((ks * 32 * 128) >> 4);
+          const uint64_t bv = pb + static_cast<uint64_t>((ks * 4 * C::kPLbo) >> 4);
+          mma_ss_f8(d, av, bv, kIdPV, (c | ks) != 0 ? 1u : 0u);
+          if constexpr (!C::kConcat)  // the lo term: the next NR / 16 core matrices
+            mma_ss_f8(d, av, bv + static_cast<uint64_t>((NR / 16 * 128) >> 4), kIdPV, 1u);
+        }
+        mma_commit(x.bar(kEmpty + slot));  // the value box's last read
+      }
+      mma_commit(x.bar(kPFree + b));
+    }
+  }
+  if (ok && x.n_chunks > 0) mma_commit(x.bar(kOFull));
+  mma_commit(x.bar(kDrain));
+  drain_wait(x, x.bar(kDrain), 0, 25);
+}
+
+// ------------------------------------------------------------------ softmax + epilogue
+// Loads NW consecutive 32-bit TMEM columns of this warp's lane quarter.
+template <int NW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[NW]) {
+  static_assert(NW % 8 == 0, "8-column units");
+#pragma unroll
+  for (int u = 0; u < NW / 8; ++u) {
+    uint32_t r[8];
+    tmem_ld_32x32b_x8(taddr + 8 * u, r);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[8 * u + i] = __uint_as_float(r[i]);
+  }
+}
+
+// p of two rows as two e4m3 code pairs: hi = e4m3(p), lo = e4m3(p - hi),
+// formed in f16 (p rounded to 11 bits first; the difference is then exact).
+__device__ __forceinline__ void p_terms(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const __half2 ph = __floats2half2_rn(p0, p1);
+  const uint32_t phb = *reinterpret_cast<const uint32_t*>(&ph);
+  uint16_t h16, l16;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;\n" : "=h"(h16) : "r"(phb));
+  uint32_t back;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(back) : "h"(h16));
+  const __half2 d = __hsub2(ph, *reinterpret_cast<const __half2*>(&back));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;\n" : "=h"(l16) : "r"(*reinterpret_cast<const uint32_t*>(&d)));
+  hi = h16;
+  lo = l16;
+}
+
+// Eight warps: warp w owns the keys of TMEM lane quarter w % 4 and the rows
+// [h NH, (h + 1) NH) of the tile, h = (w - 4) / 4, NH = NR / 2.
+template <int NR>
+__device__ void softmax_rows(const Ctx& x, const DecodeParams& p) {
+  using C = HnCfg<NR>;
+  constexpr int NH = NR / 2;
+  const int lane = x.lane;
+  const int sw = x.warp - 4;                    // softmax warp 0..7
+  const int q4 = x.warp & 3;                    // TMEM lane quarter of this warp
+  const int r0 = (sw >> 2) * NH;                // first row of this warp
+  const int k = q4 * 32 + lane;                 // the chunk key (S^T lane) this thread owns
+  const int t8 = sw * 32 + lane;                // owner of row t8 in the exchanges
+  const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+  float* wmax = reinterpret_cast<float*>(x.smem + kOffWmax);
+  float* mref = reinterpret_cast<float*>(x.smem + kOffMref);
+  float* mtrue = reinterpret_cast<float*>(x.smem + kOffMtrue);
+  float* alpha = reinterpret_cast<float*>(x.smem + kOffAlpha);
+  int* resc = reinterpret_cast<int*>(x.smem + kOffResc);
+  const int* vis = reinterpret_cast<const int*>(x.smem + kOffVis);
+  const float scale2 = p.score_scale_log2;
+  const int vis_min = vis[0];                   // row 0 of the tile has the earliest causal end
+  uint8_t* pbuf0 = x.smem + C::kOffP + (k >> 3) * C::kPLbo + (k & 7) * 16;
+  float l[NH];
+#pragma unroll
+  for (int n = 0; n < NH; ++n) l[n] = 0.f;
+  bool ok = true;
+  for (int c = 0; c < x.n_chunks && ok; ++c) {
+    const int b = c & 1;
+    const uint32_t par = (c >> 1) & 1;
+    ok = warp_wait(x, x.bar(kSFull + b), par, 31);
+    if (!ok) break;
+    fence_after_sync();
+    float s[NH];  // raw scores q.k of this key for the warp's rows
+    tmem_ld_cols<NH>(x.tbase + lane_off + C::kSCol + b * NR + r0, s);
+    tmem_ld_wait();
+    fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(x.bar(kSFree + b));  // QK^T of chunk c + 2 may overwrite it
+    // keys that exist (inside the segment) and that each row may see; a
+    // chunk inside the segment and before every row's causal end needs no mask
+    const int pos = x.seg_start + c * kKeys + k;
+    const bool key_ok = pos < x.seg_end;
+    const int chunk_end = x.seg_start + (c + 1) * kKeys;
+    const bool causal = x.qlen > 1 && chunk_end > vis_min;
+    if (chunk_end > x.seg_end || causal) {
+#pragma unroll
+      for (int n = 0; n < NH; ++n)
+        if (!(key_ok && (!causal || pos < vis[r0 + n]))) s[n] = -INFINITY;
+    }
+    // chunk max of every row over the raw scores (scale2 > 0): this warp's
+    // 32 keys, then the four lane quarters
+#pragma unroll
+    for (int n = 0; n < NH; ++n) {
+      const float r = warp_max_f32(s[n]);
+      if (lane == (n & 31)) wmax[(b * 4 + q4) * 64 + r0 + n] = r;
+    }
+    if (t8 == 0) resc[b] = 0;
+    ok = cross_sync(x, kXA + b, par, 32);
+    if (!ok) break;
+    if (t8 < NR) {
+      const float* w = wmax + b * 256 + t8;
+      const float mc = fmaxf(fmaxf(w[0], w[64]), fmaxf(w[128], w[192])) * scale2;
+      mtrue[t8] = fmaxf(mtrue[t8], mc);
+      const float mo = mref[t8];
+      float a = 1.f;
+      if (mc > mo + kMove) {  // also when the row's first visible key arrives
+        if (mo != -INFINITY) {
+          a = fast_exp2(mo - mc);
+          resc[b] = 1;
+        }
+        mref[t8] = mc;
+      }
+      alpha[b * 64 + t8] = a;
+    }
+    ok = cross_sync(x, kXB + b, par, 33);
+    if (!ok) break;
+    if (resc[b] != 0) {
+      // some rows' reference moved: their sums and O^T columns are rescaled
+#pragma unroll
+      for (int n = 0; n < NH; ++n) l[n] *= alpha[b * 64 + r0 + n];
+      if (c > 0) {  // O^T holds P.V of chunks < c: wait for the last of them
+        ok = warp_wait(x, x.bar(kPFree + ((c - 1) & 1)), ((c - 1) >> 1) & 1, 34);
+        if (!ok) break;
+        fence_after_sync();
+#pragma unroll 1
+        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+          for (int t = 0; t < (C::kConcat ? 2 : 1); ++t) {  // hi and lo columns
+            const uint32_t ta = x.tbase + lane_off + m * C::kNpv + t * NR + r0;
+#pragma unroll
+            for (int u = 0; u < NH / 8; ++u) {
+              uint32_t r[8];
+              tmem_ld_32x32b_x8(ta + 8 * u, r);
+              tmem_ld_wait();
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha[b * 64 + r0 + 8 * u + i]);
+              tmem_st_32x32b_x8(ta + 8 * u, r);
+            }
+          }
+        }
+        tmem_st_wait();
+      }
+    }
+    // the P^T buffer is free once P.V of the chunk that used it last (c - 2,
+    // or c - 1 with a single buffer) has read it
+    if (c >= C::kPBufs) {
+      const int cp = c - C::kPBufs;
+      ok = warp_wait(x, x.bar(kPFree + (cp & 1)), (cp >> 1) & 1, 35);
+      if (!ok) break;
+    }
+    // p = 2^(s scale2 - m_ref + bias) as hi + lo e4m3 terms; rows in units of
+    // 8 (an 8-byte half of a 16-row core matrix row)
+    uint8_t* pk = pbuf0 + (b % C::kPBufs) * C::kPBytes;
+#pragma unroll
+    for (int u = 0; u < NH / 8; ++u) {
+      const int R = r0 + 8 * u;  // first row of the unit
+      uint32_t hw[2], lw[2];
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint32_t hc[2], lc[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int n = 8 * u + 4 * q + 2 * e;  // row index within the warp's rows
+          const float2 m2 = *reinterpret_cast<const float2*>(mref + r0 + n);
+          const float b0 = m2.x == -INFINITY ? 0.f : m2.x - kPBias;
+          const float b1 = m2.y == -INFINITY ? 0.f : m2.y - kPBias;
+          const float p0 = fast_exp2(fmaf(s[n], scale2, -b0));
+          const float p1 = fast_exp2(fmaf(s[n + 1], scale2, -b1));
+          l[n] += p0;
+          l[n + 1] += p1;
+          p_terms(p0, p1, hc[e], lc[e]);
+        }
+        hw[q] = hc[0] | (hc[1] << 16);
+        lw[q] = lc[0] | (lc[1] << 16);
+      }
+      uint8_t* dst = pk + (R >> 4) * 128 + (R & 8);
+      *reinterpret_cast<uint2*>(dst) = make_uint2(hw[0], hw[1]);
+      *reinterpret_cast<uint2*>(dst + (NR / 16) * 128) = make_uint2(lw[0], lw[1]);
+    }
+    if (!key_ok) {
+      // a key past the segment: its value row (stale or unloaded ring
+      // contents, or cache rows past the sequence) must not reach O^T
+      // through p = 0, so it is zeroed; each row half zeroes two of the
+      // chunk's four value boxes
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int mm = 0; mm < 2; ++mm) {
+        const int m = 2 * (sw >> 2) + mm;
+        uint4* row = reinterpret_cast<uint4*>(x.smem + C::kOffRing +
+                                              ((c * kBoxes + m) % C::kSlots) * kSlot + k * 128);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) row[q] = z;
+      }
+    }
+    fence_proxy_async_smem();
+    fence_before_sync();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(x.bar(kPFull + b));
+  }
+
+  // ------------------------------------------------------------ epilogue
+  float* lsum = reinterpret_cast<float*>(x.smem + kOffLsum);
+  float* mult = reinterpret_cast<float*>(x.smem + kOffMult);
+  if (ok && x.n_chunks > 0) {
+    ok = warp_wait(x, x.bar(kOFull), 0, 36);
+    fence_after_sync();
+  }
+  if (ok) {
+#pragma unroll
+    for (int n = 0; n < NH; ++n) {
+      float v = l[n];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == (n & 31)) lsum[q4 * 64 + r0 + n] = v;
+    }
+    ok = cross_sync(x, kXE, 0, 37);
+  }
+  if (ok && t8 < NR) {
+    const int rho = x.row0 + t8;
+    const float L = (lsum[t8] + lsum[64 + t8]) + (lsum[128 + t8] + lsum[192 + t8]);
+    const float base = mref[t8] == -INFINITY ? 0.f : mref[t8] - kPBias;  // the sums' reference
+    float f = 0.f;
+    if (rho < x.rows_total) {
+      const int tok = x.tok0 + rho / x.H;
+      const int head = rho % x.H;
+      const int64_t th = static_cast<int64_t>(tok) * x.H + head;
+      if (x.fin) {
+        float lse = -INFINITY;
+        if (p.sinks != nullptr) {
+          const float s2 = p.sinks[head] * kLog2e;
+          const float M = fmaxf(L > 0.f ? base : -INFINITY, s2);
+          const float e = L > 0.f ? exp2f(base - M) : 0.f;
+          const float W = L * e + exp2f(s2 - M);
+          f = e / W;
+          lse = kLn2 * (M + log2f(W));
+        } else if (L > 0.f) {
+          f = 1.f / L;
+          lse = kLn2 * (base + log2f(L));
+        }
+        p.lse[th] = lse;
+      } else {
+        const int64_t ts = x.pslot >= 0 ? static_cast<int64_t>(x.pslot) * NR + t8
+                                        : th * p.num_segments + x.seg;
+        const float mt = mtrue[t8];
+        p.segm_max[ts] = L > 0.f ? mt : -INFINITY;
+        p.segm_expsum[ts] = L > 0.f ? L * exp2f(base - mt) : 0.f;
+        f = L > 0.f ? 1.f / L : 0.f;
+      }
+    }
+    mult[t8] = f * p.kv_scale;
+  }
+  if (ok) ok = cross_sync(x, kXF, 0, 38);
+  if (!ok) return;
+  // O^T: lane = value column, column = row; each warp instruction stores 32
+  // consecutive values of one row
+  const int rows_here = min(NR, x.rows_total - x.row0);
+#pragma unroll 1
+  for (int m = 0; m < 4; ++m) {
+    const int col = m * 128 + k;
+#pragma unroll 1
+    for (int u = 0; u < NH / 8; ++u) {
+      const int ru = r0 + 8 * u;  // first row of the 8-row unit
+      if (ru >= rows_here) break;
+      float o[8];
+      if (x.n_chunks > 0) {
+        tmem_ld_cols<8>(x.tbase + lane_off + m * C::kNpv + ru, o);
+        if constexpr (C::kConcat) {  // the lo terms' columns
+          float o2[8];
+          tmem_ld_cols<8>(x.tbase + lane_off + m * C::kNpv + NR + ru, o2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) o[i] += o2[i];
+        } else {
+          tmem_ld_wait();
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = 0.f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = ru + i;
+        if (rr >= rows_here) break;
+        const int rho = x.row0 + rr;
+        const int64_t th = static_cast<int64_t>(x.tok0 + rho / x.H) * x.H + rho % x.H;
+        const float v = o[i] * mult[rr];
+        if (x.fin) {
+          static_cast<__nv_bfloat16*>(p.out)[th * kRank + col] = __float2bfloat16_rn(v);
+        } else {
+          const int64_t ts = x.pslot >= 0 ? static_cast<int64_t>(x.pslot) * NR + rr
+                                          : th * p.num_segments + x.seg;
+          p.segm_out[ts * kRank + col] = v;
+        }
+      }
+    }
+  }
+}
+
+template <int NR>
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_hn_kernel(const __grid_constant__ HnMaps maps, const DecodeParams p, int* status) {
+  using C = HnCfg<NR>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  Ctx x;
+  x.smem = smem;
+  x.status = status;
+  x.limit_ns = p.wait_ns != 0 ? p.wait_ns : kDefaultWaitNs;
+  x.tid = threadIdx.x;
+  x.warp = x.tid >> 5;
+  x.lane = x.tid & 31;
+  int tile, item_begin = 0, item_end = 0;
+  x.pslot = -1;
+  if (p.items != nullptr) {
+    // balanced schedule: the item this CTA runs, once the grid that wrote
+    // the list (launched just before) has completed
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    // the merge grid may launch once every CTA of this one has started
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    const int item = blockIdx.x;
+    if (item >= *p.n_items) return;
+    const int4 a = reinterpret_cast<const int4*>(p.items)[2 * item];
+    const int4 b = reinterpret_cast<const int4*>(p.items)[2 * item + 1];
+    x.unit = a.x;
+    tile = a.y;
+    item_begin = a.z;
+    item_end = a.w;
+    x.pslot = b.x;
+    x.seg = 0;
+    x.fin = x.pslot < 0;
+  } else {
+    tile = blockIdx.x;
+    x.seg = blockIdx.y;
+    x.unit = blockIdx.z;
+    x.fin = p.final_mode != 0;
+  }
+  x.H = p.num_heads;
+  x.qlen = 1;
+  x.tok0 = x.unit;
+  if (p.qo_indptr != nullptr) {
+    x.tok0 = p.qo_indptr[x.unit];
+    x.qlen = p.qo_indptr[x.unit + 1] - x.tok0;
+  }
+  x.part_len = p.seq_lens[x.unit];
+  x.rows_total = x.qlen * x.H;
+  x.row0 = tile * NR;
+  if (x.row0 >= x.rows_total) return;
+  if (p.items != nullptr) {
+    x.seg_start = item_begin;
+    x.seg_end = min(item_end, x.part_len);
+  } else {
+    const int span = p.num_segments * p.tile_size;
+    const int tps = x.part_len > 0 ? cdiv(x.part_len, span) : 0;
+    const int seg_len = tps * p.tile_size;
+    x.seg_start = x.seg * seg_len;
+    x.seg_end = min(x.seg_start + seg_len, x.part_len);
+  }
+  x.n_chunks = x.seg_end > x.seg_start ? cdiv(x.seg_end - x.seg_start, kKeys) : 0;
+
+  x.bar0 = smem_u32(smem + kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + kOffTslot);
+  x.abort = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  if (x.tid == 0) {
+    *x.abort = 0;
+    for (int s = 0; s < C::kSlots; ++s) {
+      mbar_init(x.bar(kFull + s), 1);
+      mbar_init(x.bar(kEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(x.bar(kSFull + b), 1);
+      mbar_init(x.bar(kSFree + b), kSoftWarps);
+      mbar_init(x.bar(kPFull + b), kSoftWarps);
+      mbar_init(x.bar(kPFree + b), 1);
+      mbar_init(x.bar(kXA + b), kSoftWarps);
+      mbar_init(x.bar(kXB + b), kSoftWarps);
+    }
+    mbar_init(x.bar(kQFull), 1);
+    mbar_init(x.bar(kXE), kSoftWarps);
+    mbar_init(x.bar(kXF), kSoftWarps);
+    mbar_init(x.bar(kOFull), 1);
+    mbar_init(x.bar(kDrain), 1);
+    fence_barrier_init();
+  }
+  if (x.tid <= kMaxSlots) reinterpret_cast<int*>(smem + kOffIssued)[x.tid] = -1;
+  if (x.tid < 64) {
+    // per-row state: reference and true maxima, causal end of the row
+    reinterpret_cast<float*>(smem + kOffMref)[x.tid] = -INFINITY;
+    reinterpret_cast<float*>(smem + kOffMtrue)[x.tid] = -INFINITY;
+    const int rho = x.row0 + x.tid;
+    reinterpret_cast<int*>(smem + kOffVis)[x.tid] =
+        rho < x.rows_total ? x.part_len - x.qlen + rho / x.H + 1 : x.part_len;
+  }
+  if (x.warp == 1) {
+    tmem_alloc(smem_u32(tslot), C::kTmemAlloc);
+    tmem_relinquish();
+  }
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  x.tbase = *tslot;
+
+  if (x.warp == 0 || x.warp == 2 || x.warp == 3) {
+    produce<NR>(x, maps, p, x.warp == 0 ? 0 : x.warp - 1);
+  } else if (x.warp == 1) {
+    mma_issue<NR>(x);
+  } else {
+    softmax_rows<NR>(x, p);
+  }
+
+  __syncwarp();
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (x.warp == 1) tmem_dealloc(x.tbase, C::kTmemAlloc);
+  // every TMA load issued must have landed before the CTA's shared memory is
+  // released: the latest use issued in each slot (all are consumed unless the
+  // CTA aborted) and q
+  if (x.tid == 0) {
+    const volatile int* issued = reinterpret_cast<const volatile int*>(smem + kOffIssued);
+    for (int s = 0; s < C::kSlots; ++s)
+      if (issued[s] >= 0) drain_wait(x, x.bar(kFull + s), issued[s] & 1, 12);
+    if (issued[kMaxSlots] >= 0) drain_wait(x, x.bar(kQFull), 0, 13);
+  }
+}
+
+template <int NR>
+cudaError_t launch_rows(const HnMaps& maps, const DecodeParams& p, dim3 grid, int* status,
+                        cudaStream_t stream) {
+  using C = HnCfg<NR>;
+  static std::atomic<uint64_t> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(done.load(std::memory_order_acquire) & bit)) {
+    e = cudaFuncSetAttribute(decode_hn_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    done.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  if (p.items == nullptr) {
+    decode_hn_kernel<NR><<<grid, kThreads, C::kSmem, stream>>>(maps, p, status);
+    return cudaGetLastError();
+  }
+  // balanced schedule: programmatic dependent launch after the schedule kernel
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_hn_kernel<NR>, maps, p, status);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_hn(const DecodeParams& p, int rows, int64_t q_rows, int64_t kv_rows,
+                             dim3 grid, int* status, cudaStream_t stream) {
+  if (p.slots != nullptr) return cudaErrorNotSupported;
+  HnMaps maps{};
+  cudaError_t e = make_row_map(&maps.q, p.q, static_cast<uint64_t>(q_rows), static_cast<uint32_t>(rows), true);
+  if (e != cudaSuccess) return e;
+  e = make_row_map(&maps.kv, p.kv, static_cast<uint64_t>(kv_rows), kHalf, true);
+  if (e != cudaSuccess) return e;
+  switch (rows) {
+    case 16: return launch_rows<16>(maps, p, grid, status, stream);
+    case 32: return launch_rows<32>(maps, p, grid, status, stream);
+    case 48: return launch_rows<48>(maps, p, grid, status, stream);
+    case 64: return launch_rows<64>(maps, p, grid, status, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mla

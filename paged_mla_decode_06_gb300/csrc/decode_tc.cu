@@ -41,6 +41,7 @@
 #include "common.cuh"
 #include "internal.h"
 #include "tc_ops.cuh"
+#include "tma_map.cuh"
 
 namespace mla {
 namespace {
@@ -1044,37 +1045,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
   if (x.warp == 1) tmem_dealloc(x.tbase, kTmemCols);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::atomic<bool> tried{false};
-  if (!tried.load(std::memory_order_acquire)) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    tried.store(true, std::memory_order_release);
-  }
-  return fn;
-}
-
-// 2-D map over a [rows, 576] tensor with 128-byte-wide boxes of box_rows rows.
-cudaError_t make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows, bool fp8) {
-  auto enc = encode_fn();
-  if (enc == nullptr) return cudaErrorNotSupported;
-  const uint32_t elt = fp8 ? 1 : 2;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim) * elt};
-  cuuint32_t box[2] = {128 / elt, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <bool FP8, bool SPARSE>
 cudaError_t launch_variant(const TcMaps& maps, const DecodeParams& p, dim3 grid, int* status,
                            cudaStream_t stream) {
@@ -1118,13 +1088,13 @@ int decode_tc_smem_bytes(bool fp8) {
 cudaError_t launch_decode_tc(const DecodeParams& p, bool fp8, int64_t q_rows, int64_t kv_rows,
                              dim3 grid, int* status, cudaStream_t stream) {
   TcMaps maps{};
-  cudaError_t e = make_map(&maps.q, p.q, static_cast<uint64_t>(q_rows), kRows, fp8);
+  cudaError_t e = make_row_map(&maps.q, p.q, static_cast<uint64_t>(q_rows), kRows, fp8);
   if (e != cudaSuccess) return e;
-  e = make_map(&maps.kv, p.kv, static_cast<uint64_t>(kv_rows), kKeys, fp8);
+  e = make_row_map(&maps.kv, p.kv, static_cast<uint64_t>(kv_rows), kKeys, fp8);
   if (e != cudaSuccess) return e;
   if (p.slots != nullptr) {
     if (fp8) return cudaErrorNotSupported;
-    e = make_map(&maps.kv1, p.kv, static_cast<uint64_t>(kv_rows), 1, false);
+    e = make_row_map(&maps.kv1, p.kv, static_cast<uint64_t>(kv_rows), 1, false);
     if (e != cudaSuccess) return e;
     return launch_variant<false, true>(maps, p, grid, status, stream);
   }

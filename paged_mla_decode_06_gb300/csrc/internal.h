@@ -13,6 +13,7 @@ enum KernelId : int32_t {
   kMmaRows32 = 2,   // 32 rows per CTA
   kMmaRows64 = 3,   // 64 rows per CTA
   kTcPair128 = 4,   // tcgen05 CTA-pair kernel, 128 rows per pair
+  kTcRowsN = 5,     // tcgen05 kernel with the query rows as N, 16..64 rows per CTA
 };
 
 struct DecodeParams {
@@ -40,6 +41,9 @@ struct DecodeParams {
   // at items[8 i ..]; null selects the uniform NS partition
   const int32_t* items;
   const int32_t* n_items;
+  // bounded waits of the tensor-core kernels give up after this many
+  // nanoseconds (0: the default, 2 s)
+  uint64_t wait_ns;
 };
 
 // Balanced work list (sched.cu).
@@ -49,6 +53,7 @@ struct SchedParams {
   const int32_t* slot_indptr;    // sparse [T+1] or null (topk per token)
   int32_t topk, sparse, num_units, num_heads, tiles_max;
   int32_t split_cap;             // item budget when segments are split
+  int32_t tile_rows;             // query rows per row tile (and per partial slot)
   int32_t* items;                // [max_items, 8]
   int32_t* n_items;              // [1]
   int32_t* unit_tab;             // [num_units * tiles_max, 2]: first partial slot (-1), pieces
@@ -80,6 +85,7 @@ struct MergeParams {
   // each (unit, row tile) its first slot and piece count (null: uniform NS)
   const int32_t* unit_tab;
   int32_t tiles_max;
+  int32_t tile_rows;   // rows per row tile and per partial slot
   int32_t sparse;
 };
 
@@ -126,6 +132,11 @@ cudaError_t launch_fit_kpool(const int32_t* ti, int64_t ti_stride, int32_t num_t
 // and cache tensors viewed as [rows, 576]; status (may be null) receives a
 // nonzero code if a bounded wait times out.
 cudaError_t launch_decode_tc(const DecodeParams& p, bool fp8, int64_t q_rows, int64_t kv_rows,
+                             dim3 grid, int* status, cudaStream_t stream);
+
+// tcgen05 kernel with the query rows as the MMA N dimension (e4m3, dense,
+// block size a multiple of 64): rows = 16, 32, 48 or 64 query rows per CTA.
+cudaError_t launch_decode_hn(const DecodeParams& p, int rows, int64_t q_rows, int64_t kv_rows,
                              dim3 grid, int* status, cudaStream_t stream);
 
 // Shared memory bytes a decode variant needs (host query for validation).

@@ -55,20 +55,21 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
   const float sink2 = p.sinks != nullptr ? p.sinks[h] * kLog2e : -INFINITY;
   __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) + gw * p.rank;
   if (p.unit_tab != nullptr) {
-    // balanced schedule: the rows of a (unit, 128-row tile) split into k > 1
-    // pieces own k consecutive slots of 128 rows; k == 1 rows were written
-    // by the decode kernel itself
+    // balanced schedule: the rows of a (unit, row tile) split into k > 1
+    // pieces own k consecutive slots of tile_rows rows; k == 1 rows were
+    // written by the decode kernel itself
     int u = t, tok0 = t;
     if (!p.sparse && p.part.qo_indptr != nullptr) {
       u = request_of(p.part, t);
       tok0 = p.part.qo_indptr[u];
     }
     const int r = (t - tok0) * p.num_heads + h;
-    if (r / 128 >= p.tiles_max) return;
-    const int2 e = reinterpret_cast<const int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + r / 128];
+    const int tr = p.tile_rows;
+    if (r / tr >= p.tiles_max) return;
+    const int2 e = reinterpret_cast<const int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + r / tr];
     if (e.y <= 1) return;
-    merge_row<VPL, true>(p.segm_out, p.segm_max, p.segm_expsum, static_cast<int64_t>(e.x) * 128 + r % 128,
-                         128, e.y, sink2, out, p.lse + gw, lane);
+    merge_row<VPL, true>(p.segm_out, p.segm_max, p.segm_expsum, static_cast<int64_t>(e.x) * tr + r % tr,
+                         tr, e.y, sink2, out, p.lse + gw, lane);
     return;
   }
   const int NS = p.num_segments;

@@ -6,20 +6,22 @@
 // reduce_partial_map) on its persistent path.
 //
 // One block of 256 threads. A row is a (unit, row tile) pair, a unit being
-// a request of the dense variant or a token of the sparse one; a row covers
+// a request of the dense variant or a token of the sparse one, a row tile
+// the query rows one CTA (pair) of the decode owns; a row covers
 // the unit's g = cdiv(len, 128) key groups. The rows are laid end to end
 // (unit-major) and the sequence of all their groups is cut every W =
-// cdiv(total, pairs) groups, as if each CTA pair took the next W groups;
+// cdiv(total, workers) groups, as if each worker (a CTA pair of the
+// 128-row kernel, a CTA of the rows-as-N kernel) took the next W groups;
 // a cut closer than W / 8 to either end of its row is dropped, so that no
 // piece is a sliver. Every row thus becomes k >= 1 pieces (one, of size 0,
 // for an empty row, whose rows still get zeros and -inf). Items are written
-// longest first: CTA pairs are handed out in launch order, so the pairs that
+// longest first: workers are handed out in launch order, so the ones that
 // finish early take the short pieces (longest-processing-time list
 // scheduling). Pieces of a split row write base-2 partials to consecutive
 // partial slots; the unit table gives each row its first slot and its piece
 // count, from which the merge finds them. Cuts number
-// fewer than the pairs, so the slots of split rows number at most two per
-// pair and the items at most rows + pairs.
+// fewer than the workers, so the slots of split rows number at most two per
+// worker and the items at most rows + workers.
 #include "common.cuh"
 #include "internal.h"
 
@@ -47,7 +49,7 @@ __device__ __forceinline__ UnitInfo unit_info_global(const SchedParams& p, int u
   UnitInfo i;
   i.groups = len > 0 ? cdiv(len, kGroupKeys) : 0;
   const int64_t rows = static_cast<int64_t>(qlen > 0 ? qlen : 0) * p.num_heads;
-  const int64_t tiles = (rows + 127) / 128;
+  const int64_t tiles = (rows + p.tile_rows - 1) / p.tile_rows;
   i.tiles = static_cast<int>(tiles < p.tiles_max ? tiles : p.tiles_max);
   return i;
 }
@@ -231,8 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams
     total += static_cast<long long>(i.tiles) * i.groups;
   }
   total = block_sum(total, red);  // (its barriers also publish the cache)
-  const long long pairs = p.split_cap / 2 > 0 ? p.split_cap / 2 : 1;
-  const long long W = total > 0 ? (total + pairs - 1) / pairs : 1;
+  const long long workers = p.split_cap / 2 > 0 ? p.split_cap / 2 : 1;
+  const long long W = total > 0 ? (total + workers - 1) / workers : 1;
   if (total < (1ll << 30))
     schedule_items<int>(p, info, static_cast<int>(W), red, hist, start);
   else

@@ -118,7 +118,11 @@ def test_plan_sparse(lib):
     (dict(max_qlen=0), B.MLA_ERR_INVALID_ARG),
     (dict(mixed_dtype=True), B.MLA_ERR_UNSUPPORTED),
     (dict(kernel=2, block_size=16, max_blocks_per_req=600), B.MLA_ERR_UNSUPPORTED),
-    (dict(kernel=3), B.MLA_ERR_INVALID_ARG),
+    (dict(kernel=3), B.MLA_ERR_UNSUPPORTED),              # rows-as-N: e4m3 only
+    (dict(kernel=3, dtype="fp8"), B.MLA_ERR_UNSUPPORTED), # rows-as-N: 128 heads > 64 rows
+    (dict(kernel=3, dtype="fp8", num_heads=16, block_size=16, max_blocks_per_req=600),
+     B.MLA_ERR_UNSUPPORTED),                              # rows-as-N: block size not 64k
+    (dict(kernel=4), B.MLA_ERR_INVALID_ARG),
 ])
 def test_plan_rejects(lib, kw, status):
     kw = dict(kw)
@@ -256,6 +260,27 @@ def test_plan_balanced_schedule(lib):
     assert B.mla_decode_plan(_dense_problem(kernel=B.MLA_KERNEL_WARP_MMA)).schedule == 0
 
 
+@pytest.mark.parametrize("heads,qlen,rows", [(16, 1, 16), (20, 1, 32), (32, 1, 32), (48, 1, 48),
+                                             (64, 1, 64), (16, 4, 64), (20, 3, 64), (1, 1, 16)])
+def test_plan_rows_as_n(lib, heads, qlen, rows):
+    """e4m3 requests of at most 64 query rows go to the rows-as-N kernel (one
+    CTA per row tile, one worker per SM under the balanced schedule, partial
+    slots of rows_per_cta rows); wider ones stay on the CTA pair."""
+    prob = _dense_problem(dtype="fp8", num_heads=heads, num_tokens=64 * qlen, max_qlen=qlen)
+    plan = B.mla_decode_plan(prob)
+    assert plan.kernel == 5 and plan.rows_per_cta == rows and plan.row_tiles == 1
+    assert plan.schedule == 1 and plan.split_items == 2 * 152 and plan.max_items == 64 + 152
+    slot_rows = plan.split_items * rows
+    assert plan.segm_max_offset - plan.segm_output_offset >= slot_rows * 512 * 4
+    assert plan.workspace_bytes >= plan.segm_expsum_offset + slot_rows * 4
+    assert plan.workspace_bytes <= 64 << 20
+    # the CTA pair and the warp-MMA kernel can still be asked for
+    assert B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=heads, num_tokens=64 * qlen,
+                                            max_qlen=qlen, kernel=B.MLA_KERNEL_TCGEN05)).kernel == 4
+    wide = B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=65))
+    assert wide.kernel == 4
+
+
 def test_schedule_stages_reject_bad_arguments(lib):
     plan = B.mla_decode_plan(_dense_problem())
     uniform = B.mla_decode_plan(_dense_problem(num_segments=4))
@@ -339,12 +364,17 @@ def test_plan_random_problems_are_consistent(lib):
         assert plan.num_segments >= 1 and plan.tile_size >= 1 and plan.row_tiles >= 1
         assert plan.grid_x >= 1 and plan.grid_y >= 1 and plan.grid_z == units
         assert plan.workspace_bytes >= 256 and plan.workspace_bytes % 256 == 0
+        rn_ok = (not sparse and prob.kv_dtype == B.MLA_DTYPE_FP8_E4M3 and bs % 64 == 0
+                 and heads * prob.max_qlen <= 64)
+        if rn_ok:  # the planner's first choice wherever it can run
+            assert plan.kernel == 5 and plan.rows_per_cta == -(-heads * prob.max_qlen // 16) * 16
+            assert plan.row_tiles == 1 and plan.grid_x == 1
         if plan.schedule == 1:
-            assert plan.kernel == 4 and ns == 0 and plan.num_segments == 1
-            pairs = max(1, sms // 2)
-            assert plan.split_items == 2 * pairs
-            assert plan.max_items == units * plan.row_tiles + pairs
-            rows = plan.split_items * 128
+            assert plan.kernel in (4, 5) and ns == 0 and plan.num_segments == 1
+            workers = max(1, sms // 2) if plan.kernel == 4 else sms
+            assert plan.split_items == 2 * workers
+            assert plan.max_items == units * plan.row_tiles + workers
+            rows = plan.split_items * plan.rows_per_cta
             assert plan.segm_output_offset >= 512 + plan.max_items * 32
             assert plan.segm_max_offset >= plan.segm_output_offset + rows * 512 * 4
             assert plan.segm_expsum_offset >= plan.segm_max_offset + rows * 4
