@@ -29,8 +29,8 @@
 // only when a chunk max exceeds it by more than 4 (O^T is then rescaled in
 // TMEM), so p <= 2^8 fits e4m3 and the bulk of the weights stays in its
 // normal range; the true max is kept for the partials.
-// Warps: 0, 2, 3 TMA producers (q; the key boxes through the block table), 1
-// MMA issue, 4-11 softmax and epilogue (a lane quarter of keys and half of
+// Warps: 0, 2 TMA producers (q; the key boxes through the block table), 1
+// QK^T issue, 3 P.V issue, 4-11 softmax and epilogue (a lane quarter of keys and half of
 // the rows each, two warps per SM sub-partition). Every wait is bounded: a timeout
 // records a code in the status word, stops the CTA's work, drains what it
 // issued and exits.
@@ -52,7 +52,7 @@ constexpr int kHalf = 64;                // keys per TMA box (rows of one block)
 constexpr int kSlot = kKeys * 128;       // ring slot: one 128-byte column box of a chunk
 constexpr int kBoxes = 5;                // per chunk: 4 latent boxes (512 e4m3) + the rope box
 constexpr int kThreads = 384;
-constexpr int kProducers = 3;            // warps 0, 2, 3
+constexpr int kProducers = 2;            // warps 0, 2
 constexpr int kSoftWarps = 8;            // warps 4-11: four TMEM lane quarters x two row halves
 constexpr int kMaxSlots = 14;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
@@ -72,8 +72,9 @@ enum : int {
   kXE = kXB + 2,                // epilogue: row sums posted
   kXF = kXE + 1,                // epilogue: row factors posted
   kOFull = kXF + 1,             // last P.V complete
-  kDrain = kOFull + 1,
-  kNumBars = kDrain + 1
+  kDrain = kOFull + 1,          // the QK^T issuer's MMAs complete
+  kDrainPV = kDrain + 1,        // the P.V issuer's MMAs complete
+  kNumBars = kDrainPV + 1
 };
 
 // Shared-memory header: barriers, TMEM address, abort flag, exchange arrays.
@@ -149,23 +150,22 @@ __device__ __forceinline__ void report(int* status, int code) {
   if (status != nullptr) atomicCAS(status, 0, code);
 }
 
-// Bounded wait on a barrier phase; false on timeout (recorded) or abort.
+// Bounded wait on a barrier phase; false on timeout (recorded) or abort. The
+// thread sleeps in the wait (up to kSleepNs at a time, woken by the phase)
+// rather than spinning, which would take issue slots from the MMA issuer.
+constexpr uint32_t kSleepNs = 20000;
 __device__ bool wait_phase(const Ctx& x, uint32_t bar, uint32_t parity, int code) {
-  uint64_t t0 = 0;
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait_sleep(bar, parity, kSleepNs)) {
     if (*x.abort) return false;
-    if ((it & 15u) == 0) {
-      const uint64_t now = global_timer_ns();
-      if (t0 == 0) {
-        t0 = now;
-      } else if (now - t0 > x.limit_ns) {
-        report(x.status, code);
-        *x.abort = 1;
-        return false;
-      }
+    if (global_timer_ns() - t0 > x.limit_ns) {
+      report(x.status, code);
+      *x.abort = 1;
+      return false;
     }
   }
+  return true;
 }
 
 // Every lane waits (each acquires what the phase published); warp-uniform result.
@@ -176,7 +176,7 @@ __device__ __forceinline__ bool warp_wait(const Ctx& x, uint32_t bar, uint32_t p
 // Wait that ignores the abort flag (teardown drains), bounded by the default limit.
 __device__ void drain_wait(const Ctx& x, uint32_t bar, uint32_t parity, int code) {
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, kSleepNs)) {
     if (global_timer_ns() - t0 > kDefaultWaitNs) {
       report(x.status, code);
       return;
@@ -267,77 +267,87 @@ __device__ void produce(const Ctx& x, const HnMaps& maps, const DecodeParams& p,
 }
 
 // ------------------------------------------------------------------ MMA issue
-// Software-pipelined: S^T of chunk g, then O^T += V^T P^T of chunk g - 1, so
-// that the softmax of a chunk overlaps the QK^T of the next.
+// Two issuing threads on different SM sub-partitions: one issues QK^T chunk
+// after chunk as the boxes land (two S^T buffers ahead of the softmax), the
+// other P.V as soon as a chunk's P^T is written. A tcgen05.mma with N <= 64
+// takes ~40 cycles of the tensor pipe but ~95 to issue from one thread that
+// shares its sub-partition with busy softmax warps (measured); two issuers
+// keep the pipe fed, and P.V of a chunk never waits behind the next chunk's
+// loads, so its value boxes return to the ring at once.
 template <int NR>
-__device__ void mma_issue(const Ctx& x) {
+__device__ void qk_issue(const Ctx& x) {
   using C = HnCfg<NR>;
   if (x.lane != 0) return;
   constexpr uint32_t kIdQK = instr_desc(128, NR, 0, 0, false, false);
-  constexpr uint32_t kIdPV = instr_desc(128, C::kNpv, 0, 0, true, true);
   const uint64_t q_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffQ), 16, 1024);
-  const uint64_t k_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffRing), 16, 1024);      // K-major
-  const uint64_t v_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffRing), kSlot, 1024);   // MN-major
-  const uint64_t p_desc = smem_desc_interleave(smem_u32(x.smem + C::kOffP), C::kPLbo, 128);
+  const uint64_t k_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffRing), 16, 1024);  // K-major
   bool ok = x.n_chunks == 0 || wait_phase(x, x.bar(kQFull), 0, 21);
-  for (int g = 0; g <= x.n_chunks && ok; ++g) {
-    if (g < x.n_chunks) {
-      const int b = g & 1;
-      if (g >= 2 && !wait_phase(x, x.bar(kSFree + b), ((g - 2) >> 1) & 1, 22)) {
-        ok = false;
-        break;
-      }
-      const uint32_t d = x.tbase + C::kSCol + b * NR;
+  for (int c = 0; c < x.n_chunks && ok; ++c) {
+    const int b = c & 1;
+    if (c >= 2 && !wait_phase(x, x.bar(kSFree + b), ((c - 2) >> 1) & 1, 22)) break;
+    const uint32_t d = x.tbase + C::kSCol + b * NR;
 #pragma unroll
-      for (int j = 0; j < kBoxes; ++j) {
-        const int i = g * kBoxes + j;
-        const int slot = i % C::kSlots;
-        if (!wait_phase(x, x.bar(kFull + slot), (i / C::kSlots) & 1, 23)) {
-          ok = false;
-          break;
-        }
-        fence_after_sync();
-        const uint64_t a = k_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
-        const uint64_t qb = q_desc + static_cast<uint64_t>(j * (C::kQBox >> 4));
-        // 32 e4m3 columns per instruction: 4 per latent box, 2 for the 64 rope columns
-#pragma unroll
-        for (int s = 0; s < (j < 4 ? 4 : 2); ++s)
-          mma_ss_f8(d, a + 2 * s, qb + 2 * s, kIdQK, (j | s) != 0 ? 1u : 0u);
-        if (j == 4) mma_commit(x.bar(kEmpty + slot));  // the rope box's only read
-      }
-      if (!ok) break;
-      mma_commit(x.bar(kSFull + b));
-    }
-    if (g >= 1) {
-      const int c = g - 1;
-      const int b = c & 1;
-      if (!wait_phase(x, x.bar(kPFull + b), (c >> 1) & 1, 24)) {
+    for (int j = 0; j < kBoxes; ++j) {
+      const int i = c * kBoxes + j;
+      const int slot = i % C::kSlots;
+      if (!wait_phase(x, x.bar(kFull + slot), (i / C::kSlots) & 1, 23)) {
         ok = false;
         break;
       }
       fence_after_sync();
-      const uint64_t pb = p_desc + static_cast<uint64_t>((b % C::kPBufs) * (C::kPBytes >> 4));
+      const uint64_t a = k_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
+      const uint64_t qb = q_desc + static_cast<uint64_t>(j * (C::kQBox >> 4));
+      // 32 e4m3 columns per instruction: 4 per latent box, 2 for the 64 rope columns
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const int slot = (c * kBoxes + m) % C::kSlots;
-        const uint64_t a = v_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
-        const uint32_t d = x.tbase + m * C::kNpv;
-#pragma unroll
-        for (int ks = 0; ks < kKeys / 32; ++ks) {
-          const uint64_t av = a + static_cast<uint64_t>((ks * 32 * 128) >> 4);
-          const uint64_t bv = pb + static_cast<uint64_t>((ks * 4 * C::kPLbo) >> 4);
-          mma_ss_f8(d, av, bv, kIdPV, (c | ks) != 0 ? 1u : 0u);
-          if constexpr (!C::kConcat)  // the lo term: the next NR / 16 core matrices
-            mma_ss_f8(d, av, bv + static_cast<uint64_t>((NR / 16 * 128) >> 4), kIdPV, 1u);
-        }
-        mma_commit(x.bar(kEmpty + slot));  // the value box's last read
-      }
-      mma_commit(x.bar(kPFree + b));
+      for (int s = 0; s < (j < 4 ? 4 : 2); ++s)
+        mma_ss_f8(d, a + 2 * s, qb + 2 * s, kIdQK, (j | s) != 0 ? 1u : 0u);
+      if (j == 4) mma_commit(x.bar(kEmpty + slot));  // the rope box's only read
     }
+    if (!ok) break;
+    mma_commit(x.bar(kSFull + b));
   }
-  if (ok && x.n_chunks > 0) mma_commit(x.bar(kOFull));
   mma_commit(x.bar(kDrain));
   drain_wait(x, x.bar(kDrain), 0, 25);
+}
+
+template <int NR>
+__device__ void pv_issue(const Ctx& x) {
+  using C = HnCfg<NR>;
+  if (x.lane != 0) return;
+  constexpr uint32_t kIdPV = instr_desc(128, C::kNpv, 0, 0, true, true);
+  const uint64_t v_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffRing), kSlot, 1024);   // MN-major
+  const uint64_t p_desc = smem_desc_interleave(smem_u32(x.smem + C::kOffP), C::kPLbo, 128);
+  bool ok = true;
+  for (int c = 0; c < x.n_chunks && ok; ++c) {
+    const int b = c & 1;
+    // P^T of chunk c written; the softmax waited for S^T of the chunk, whose
+    // QK^T waited for the very value boxes read here
+    if (!wait_phase(x, x.bar(kPFull + b), (c >> 1) & 1, 24)) {
+      ok = false;
+      break;
+    }
+    fence_after_sync();
+    const uint64_t pb = p_desc + static_cast<uint64_t>((b % C::kPBufs) * (C::kPBytes >> 4));
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int slot = (c * kBoxes + m) % C::kSlots;
+      const uint64_t a = v_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
+      const uint32_t dm = x.tbase + m * C::kNpv;
+#pragma unroll
+      for (int ks = 0; ks < kKeys / 32; ++ks) {
+        const uint64_t av = a + static_cast<uint64_t>((ks * 32 * 128) >> 4);
+        const uint64_t bv = pb + static_cast<uint64_t>((ks * 4 * C::kPLbo) >> 4);
+        mma_ss_f8(dm, av, bv, kIdPV, (c | ks) != 0 ? 1u : 0u);
+        if constexpr (!C::kConcat)  // the lo term: the next NR / 16 core matrices
+          mma_ss_f8(dm, av, bv + static_cast<uint64_t>((NR / 16 * 128) >> 4), kIdPV, 1u);
+      }
+      mma_commit(x.bar(kEmpty + slot));  // the value box's last read
+    }
+    mma_commit(x.bar(kPFree + b));
+  }
+  if (ok && x.n_chunks > 0) mma_commit(x.bar(kOFull));
+  mma_commit(x.bar(kDrainPV));
+  drain_wait(x, x.bar(kDrainPV), 0, 26);
 }
 
 // ------------------------------------------------------------------ softmax + epilogue
@@ -712,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(x.bar(kXF), kSoftWarps);
     mbar_init(x.bar(kOFull), 1);
     mbar_init(x.bar(kDrain), 1);
+    mbar_init(x.bar(kDrainPV), 1);
     fence_barrier_init();
   }
   if (x.tid <= kMaxSlots) reinterpret_cast<int*>(smem + kOffIssued)[x.tid] = -1;
@@ -732,10 +743,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   fence_after_sync();
   x.tbase = *tslot;
 
-  if (x.warp == 0 || x.warp == 2 || x.warp == 3) {
-    produce<NR>(x, maps, p, x.warp == 0 ? 0 : x.warp - 1);
+  if (x.warp == 0 || x.warp == 2) {
+    produce<NR>(x, maps, p, x.warp >> 1);
   } else if (x.warp == 1) {
-    mma_issue<NR>(x);
+    qk_issue<NR>(x);
+  } else if (x.warp == 3) {
+    pv_issue<NR>(x);
   } else {
     softmax_rows<NR>(x, p);
   }
