@@ -53,6 +53,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
       : "memory");
   return ok != 0;
 }
+// Same, with cluster-scope acquire (barriers a peer CTA arrives on).
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Non-blocking test of a phase (never suspends the thread): for polling
 // several barriers in turn.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
