@@ -11,7 +11,14 @@ the decode over it, and the merge of the rows the list split. Inputs are
 seeded and synthetic. L2 is flushed (a 256 MiB write) before every timed
 step, and only the step itself is inside its CUDA events. The roofline's
 kernel time is the decode launch alone, timed the same way on the same work
-list.
+list; its bound is HBM when the launch's algorithmic bytes at the measured
+copy rate take longer than its flops at the dense tensor peak of its dtype
+(e4m3: the measured bf16 peak times the nominal 2x), else the tensor pipe.
+
+The default line also carries ``workloads``: the other workload shapes (the
+tiny batch, the e4m3 batch at 16 and 128 heads, multi-token rows with
+sinks, the sparse top-k decode), each timed in the same run the same way,
+with its per-call and decode times, both roofline fractions and its bound.
 
 Under torchrun (N > 1) every rank decodes its own batch of the same shape
 (weak scaling, no collective on the data path); the per-step time is the max
@@ -72,7 +79,7 @@ def _build_workload(name, seed_offset=0, batch=None, heads=128):
         b = batch or 64
         return I.dsv3_bf16(seed=2 + seed_offset, batch=b), WORKLOADS[name].format(b=b)
     if name == "tiny":
-        return I.tiny_dense(seed=1 + seed_offset), WORKLOADS[name]
+        return I.tiny_dense(seed=1 + seed_offset), WORKLOADS[name].format()
     if name == "fp8":
         b = batch or 52
         return I.fp8_decode(heads, seed=3 + seed_offset, batch=b), \
@@ -81,7 +88,7 @@ def _build_workload(name, seed_offset=0, batch=None, heads=128):
         b = batch or 32
         return I.mtp_sinks(seed=4 + seed_offset, batch=b), WORKLOADS[name].format(b=b)
     if name == "sparse":
-        return I.sparse_topk(seed=5 + seed_offset), WORKLOADS[name]
+        return I.sparse_topk(seed=5 + seed_offset), WORKLOADS[name].format()
     raise ValueError(name)
 
 
@@ -166,15 +173,30 @@ def _alg_bytes_decode(w):
     return _kv_keys(w) * _row_bytes(w) + qb + blocks * 4 + w.num_reqs * 4
 
 
+def smi_gpu_id(dev) -> str:
+    """The GPU as nvidia-smi names it: its UUID (or PCI bus id), not the CUDA
+    ordinal, which CUDA_VISIBLE_DEVICES renumbers."""
+    import torch
+    props = torch.cuda.get_device_properties(dev)
+    u = str(getattr(props, "uuid", "") or "")
+    if len(u) == 36 and u.count("-") == 4:
+        return "GPU-" + u
+    try:
+        return f"{props.pci_domain_id:08x}:{props.pci_bus_id:02x}:{props.pci_device_id:02x}.0"
+    except AttributeError:
+        return str(dev.index or 0)
+
+
 class ClockSampler:
-    """nvidia-smi sampled every 100 ms while the timed region runs."""
+    """nvidia-smi sampled every 100 ms while the timed region runs (read-only
+    queries of the one GPU the benchmark runs on)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, log_path: str | None = None):
-        self.gpu = gpu_index
+    def __init__(self, gpu_id: str, log_path: str | None = None):
+        self.gpu = gpu_id
         self.proc = None
         self.lines = []
         self.log_path = log_path
@@ -300,6 +322,42 @@ def cpu_baseline_steps(budget_s=20.0, n_steps=1):
     return recs
 
 
+def _tiny_worker(q, reps):
+    import oracle as O
+    from paged_mla_decode_06_gb300 import inputs as I
+    w = I.tiny_dense()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        O.mla_decode(w.q, "bf16", 1.0, w.cache, "bf16", 1.0, w.block_table, w.seq_lens,
+                     w.softmax_scale, block_size=w.block_size)
+    q.put({"seconds": time.perf_counter() - t0, "keys": reps * int(w.seq_lens.sum())})
+
+
+def cpu_baseline_tiny_1core(reps=20):
+    """The oracle on the tiny batch (2 requests, 16 heads, 167 keys) in a
+    spawned process limited to one BLAS thread."""
+    env_keys = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+    saved = {k: os.environ.get(k) for k in env_keys}
+    for k in env_keys:
+        os.environ[k] = "1"
+    try:
+        ctx = mp.get_context("spawn")
+        q = ctx.Queue()
+        p = ctx.Process(target=_tiny_worker, args=(q, reps))
+        p.start()
+        r = q.get(timeout=600)
+        p.join(timeout=60)
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    return {"value": r["keys"] / r["seconds"], "unit": UNIT, "cores": 1, "kind": "oracle",
+            "us_per_call": r["seconds"] / reps * 1e6,
+            "sample": f"fp64 numpy oracle, tiny_dense whole batch x {reps}, one BLAS thread"}
+
+
 def cpu_baseline(budget_s=20.0):
     return cpu_baseline_steps(budget_s, 1)[0]
 
@@ -323,6 +381,119 @@ def aggregate_over_ranks(times_ms, units, device=None):
     u = torch.tensor([float(units)], dtype=torch.float64, device=dev)
     dist.all_reduce(u, op=dist.ReduceOp.SUM)
     return [float(x) for x in t.tolist()], float(u.item())
+
+
+def tensor_peak_tflops(peaks, kv_dtype):
+    """Dense tensor peak for the arithmetic a workload runs: the measured bf16
+    GEMM peak, times the nominal e4m3:bf16 ratio (4.5 / 2.25 PFLOP/s dense)
+    for an e4m3 cache."""
+    return float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])) * (
+        2.0 if kv_dtype == "fp8" else 1.0)
+
+
+def roofline_of(w, kernel_us, peaks):
+    """Both fractions of one decode launch and the bound that applies: HBM when
+    its algorithmic bytes at the measured copy rate take longer than its
+    flops at the dtype's dense peak, else the tensor pipe."""
+    alg = _alg_bytes_decode(w)
+    flops = _flops(w)
+    bw = float(peaks["hbm_gbs"])
+    tp = tensor_peak_tflops(peaks, w.kv_dtype)
+    t_mem_us = alg / (bw * 1e9) * 1e6
+    t_tc_us = flops / (tp * 1e12) * 1e6
+    gbs = alg / (kernel_us * 1e-6) / 1e9
+    tfs = flops / (kernel_us * 1e-6) / 1e12
+    return {"bound": "hbm" if t_mem_us >= t_tc_us else "tensor",
+            "hbm_gbs": gbs, "hbm_frac": gbs / bw, "tensor_tflops": tfs,
+            "tensor_peak_tflops": tp, "tensor_frac": tfs / tp,
+            "algorithmic_bytes": alg, "algorithmic_flops": flops}
+
+
+def make_decode_only(B, dw, w, plan):
+    """The decode launch of one step alone: the kernel over the step's work
+    list (balanced plans) or the split-K stage writing its partials."""
+    import torch
+    dev = dw.device
+    T, H, NS = w.num_tokens, w.num_heads, plan.num_segments
+    so = torch.empty((T, H, NS, 512), dtype=torch.float32, device=dev)
+    sm = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
+    se = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
+    if w.sparse:
+        dw.convert()
+    balanced = plan.schedule == 1
+    if balanced:  # the work list a step computes, for the same lengths
+        B.mla_decode_schedule(plan, seq_lens=None if w.sparse else dw.seq_lens,
+                              qo_indptr=dw.qo_indptr, workspace=dw.workspace)
+
+    def decode_only():
+        if balanced:
+            B.mla_decode_items(plan, dw.q, dw.cache,
+                               block_table=None if w.sparse else dw.block_table,
+                               seq_lens=None if w.sparse else dw.seq_lens,
+                               qo_indptr=dw.qo_indptr, sparse_slots=dw.slots,
+                               softmax_scale=w.softmax_scale, q_scale=w.q_scale,
+                               kv_scale=w.kv_scale, sinks=dw.sinks, workspace=dw.workspace,
+                               out=dw.out, lse=dw.lse)
+            return
+        B.mla_decode_segments(plan, dw.q, dw.cache,
+                              block_table=None if w.sparse else dw.block_table,
+                              seq_lens=None if w.sparse else dw.seq_lens,
+                              qo_indptr=dw.qo_indptr, sparse_slots=dw.slots,
+                              softmax_scale=w.softmax_scale, q_scale=w.q_scale,
+                              kv_scale=w.kv_scale, segm_output=so, segm_max=sm, segm_expsum=se)
+    return decode_only
+
+
+def time_loop(fn, steps, flush, stream):
+    """Per-call device times (ms) of fn, L2 flushed before each, CUDA events on
+    the launching stream."""
+    import torch
+    out = []
+    for _ in range(steps):
+        flush.fill_(1)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        e1.synchronize()
+        out.append(e0.elapsed_time(e1))
+    return out
+
+
+# The other workload shapes, timed in the same run as the headline: the
+# small-case check, the e4m3 batch at the two head counts the pages quote,
+# multi-token rows with sinks, and the sparse top-k decode.
+SIDE_WORKLOADS = [("tiny", 16), ("fp8", 16), ("fp8", 128), ("mtp", 128), ("sparse", 128)]
+
+
+def side_workloads(B, dev, flush, stream, peaks, steps):
+    import torch
+    res = {}
+    for name, heads in SIDE_WORKLOADS:
+        w, desc = _build_workload(name, heads=heads)
+        dw = B.DeviceWorkload(w, device=dev)
+        plan = dw.plan
+        for _ in range(3):
+            dw.forward()
+        torch.cuda.synchronize(dev)
+        step = time_loop(dw.forward, steps, flush, stream)
+        dec_fn = make_decode_only(B, dw, w, plan)
+        for _ in range(3):
+            dec_fn()
+        dec = time_loop(dec_fn, steps, flush, stream)
+        us = statistics.mean(step) * 1e3
+        dus = statistics.mean(dec) * 1e3
+        key = f"{name}_h{heads}" if name == "fp8" else name
+        res[key] = {"workload": desc, "us_per_call": us, "decode_us": dus,
+                    "kv_tokens_per_s": _kv_keys(w) / (us * 1e-6),
+                    "kernel": int(plan.kernel), "rows_per_cta": int(plan.rows_per_cta),
+                    "schedule": "balanced" if plan.schedule == 1 else "uniform",
+                    "num_segments": int(plan.num_segments), "status_word": dw.status(),
+                    **roofline_of(w, dus, peaks)}
+        del dw, dec_fn
+        torch.cuda.empty_cache()
+    return res
 
 
 def run_gpu(args):
@@ -364,7 +535,7 @@ def run_gpu(args):
         dw.forward()
     barrier()
     # the raw clock samples go to a CSV only when MLA_BENCH_CLOCKS_CSV names one
-    sampler = ClockSampler(dev.index or 0, os.environ.get("MLA_BENCH_CLOCKS_CSV") or None)
+    sampler = ClockSampler(smi_gpu_id(dev), os.environ.get("MLA_BENCH_CLOCKS_CSV") or None)
     sampler.start()
     barrier()
     t_wall = time.perf_counter()
@@ -383,47 +554,11 @@ def run_gpu(args):
 
     # ---- the decode kernel alone (same launch as inside the step)
     T, H, NS = w.num_tokens, w.num_heads, plan.num_segments
-    so = torch.empty((T, H, NS, 512), dtype=torch.float32, device=dev)
-    sm = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
-    se = torch.empty((T, H, NS), dtype=torch.float32, device=dev)
-
-    if w.sparse:
-        dw.convert()
-
     balanced = plan.schedule == 1
-    if balanced:  # the work list the step computed, for the same lengths
-        B.mla_decode_schedule(plan, seq_lens=None if w.sparse else dw.seq_lens,
-                              qo_indptr=dw.qo_indptr, workspace=dw.workspace)
-
-    def decode_only():
-        if balanced:  # the decode kernel of the step: same launch, same work list
-            B.mla_decode_items(plan, dw.q, dw.cache,
-                               block_table=None if w.sparse else dw.block_table,
-                               seq_lens=None if w.sparse else dw.seq_lens,
-                               qo_indptr=dw.qo_indptr, sparse_slots=dw.slots,
-                               softmax_scale=w.softmax_scale, q_scale=w.q_scale,
-                               kv_scale=w.kv_scale, sinks=dw.sinks, workspace=dw.workspace,
-                               out=dw.out, lse=dw.lse)
-            return
-        B.mla_decode_segments(plan, dw.q, dw.cache,
-                              block_table=None if w.sparse else dw.block_table,
-                              seq_lens=None if w.sparse else dw.seq_lens,
-                              qo_indptr=dw.qo_indptr, sparse_slots=dw.slots,
-                              softmax_scale=w.softmax_scale, q_scale=w.q_scale,
-                              kv_scale=w.kv_scale, segm_output=so, segm_max=sm, segm_expsum=se)
-
+    decode_only = make_decode_only(B, dw, w, plan)
     for _ in range(3):
         decode_only()
-    dec_ms = []
-    for _ in range(args.steps):
-        flush.fill_(1)
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        decode_only()
-        e1.record(stream)
-        e1.synchronize()
-        dec_ms.append(e0.elapsed_time(e1))
+    dec_ms = time_loop(decode_only, args.steps, flush, stream)
     clocks = sampler.stop()
 
     # ---- end to end through the C ABI with host buffers: every step copies
@@ -473,11 +608,23 @@ def run_gpu(args):
     if rank == 0:
         peaks, src = _peaks()
         alg = _alg_bytes_decode(w)
-        achieved = alg / (dms * 1e-3) / 1e9
-        peak_bw = float(peaks["hbm_gbs"])
-        tflops = _flops(w) / (dms * 1e-3) / 1e12
-        kname = "decode_tc_kernel (tcgen05 CTA pair)" if plan.kernel == 4 else \
-            "decode_mma_kernel (warp MMA)"
+        rf = roofline_of(w, dms * 1e3, peaks)
+        kname = {4: "decode_tc_kernel (tcgen05 CTA pair, rows as M)",
+                 5: "decode_hn_kernel (tcgen05, rows as N)"}.get(int(plan.kernel),
+                                                                "decode_mma_kernel (warp MMA)")
+        if rf["bound"] == "hbm":
+            roof = {"bound": "hbm", "achieved": rf["hbm_gbs"], "peak": float(peaks["hbm_gbs"]),
+                    "unit": "GB/s", "frac": rf["hbm_frac"], "peak_source": f"hbm_gbs of {src}"}
+        else:
+            roof = {"bound": "tensor", "achieved": rf["tensor_tflops"], "peak": rf["tensor_peak_tflops"],
+                    "unit": "TFLOP/s", "frac": rf["tensor_frac"],
+                    "peak_source": f"bf16_tflops (burst) of {src}" +
+                                   (" x 2 (nominal e4m3:bf16)" if w.kv_dtype == "fp8" else "")}
+        roof.update({"traffic": _profiled_traffic(alg, int(plan.kernel), args.workload),
+                     "kernel": kname, "kernel_us": dms * 1e3, "algorithmic_bytes": alg,
+                     "algorithmic_flops": rf["algorithmic_flops"],
+                     "hbm_frac": rf["hbm_frac"], "tensor_tflops": rf["tensor_tflops"],
+                     "tensor_frac": rf["tensor_frac"]})
         line = {
             "metric": METRIC,
             "value": keys_total / (ms * 1e-3),
@@ -498,14 +645,7 @@ def run_gpu(args):
                        "kv_tokens_per_gpu": int(keys_rank),
                        "l2": "flushed (256 MiB write) before every timed step",
                        "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak_bw, "unit": "GB/s",
-                         "frac": achieved / peak_bw,
-                         "traffic": _profiled_traffic(alg, int(plan.kernel), args.workload),
-                         "kernel": kname,
-                         "kernel_us": dms * 1e3, "algorithmic_bytes": alg,
-                         "peak_source": f"hbm_gbs of {src}",
-                         "tensor_tflops": tflops,
-                         "tensor_frac": tflops / float(peaks.get("bf16_tflops", 1900.0))},
+            "roofline": roof,
             "clocks": clocks,
             "e2e": {"value": keys_total / (ems * 1e-3), "unit": UNIT,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -515,8 +655,13 @@ def run_gpu(args):
             "status_word": dw.status(),
             "wall_s_timed_region": wall,
         }
-        if world == 1 and not args.no_cpu_baseline and args.workload == "dsv3" and not args.batch:
+        default_line = world == 1 and args.workload == "dsv3" and not args.batch
+        if default_line and not args.no_workloads:
+            line["workloads"] = side_workloads(B, dev, flush, stream, peaks,
+                                               min(args.steps, args.side_steps))
+        if default_line and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_budget)
+            line["cpu_baseline"]["tiny_1core"] = cpu_baseline_tiny_1core()
         else:
             line["cpu_baseline"] = None
         print(json.dumps(line), flush=True)
@@ -615,6 +760,10 @@ def main():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other workload shapes on the default line")
+    ap.add_argument("--side-steps", type=int, default=100,
+                    help="timed calls per workload of the workloads object")
     ap.add_argument("--kernel", default="auto", choices=["auto", "mma", "tc"],
                     help="decode kernel variant (default: the planner's choice)")
     ap.add_argument("--num-segments", type=int, default=0,
