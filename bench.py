@@ -121,13 +121,21 @@ def _flops(w):
     return float(tot) * H * 2176.0
 
 
-# DRAM bytes (read + write) per algorithmic byte of the tensor-core decode
-# kernel, from one ncu capture (the profile summary under profiles/ names the
-# command and the numbers), valid only for the kernel source it was taken on.
+# DRAM bytes (read + write) per algorithmic byte of a decode kernel, from one
+# ncu capture each (the profile summaries under profiles/ name the commands
+# and the numbers), valid only for the kernel source each was taken on and
+# the workload it was taken on: (kernel id, workload, heads) -> record.
 PROFILED_TRAFFIC = {
-    # sha256 of decode_tc.cu's code with comments and blank lines removed
-    "code_sha256": "4a941b365f12daca8f7432e53a8dafcd8ce879b33d527a4c02e4b098c05d8654",
-    "dram_per_alg_byte": (139.576320 + 3.362560) / 138.103440,
+    (4, "dsv3", None): {  # decode_tc.cu, DeepSeek-V3-shaped batch (profiles/decode_tc_dsv3.md)
+        "source": "decode_tc.cu",
+        "code_sha256": "6ed484883791543c30f67ace22adb9950df6008e8220e28377dfbfbb134d6d79",
+        "dram_per_alg_byte": (139.582976 + 3.517184) / 138.103440,
+    },
+    (5, "fp8", 16): {  # decode_hn.cu, e4m3 batch at 16 heads (profiles/decode_hn_fp8.md)
+        "source": "decode_hn.cu",
+        "code_sha256": "95e8a0df03df0c02955a6769a81b2005cd507b728945e8a4154701c0c84293d2",
+        "dram_per_alg_byte": (226.840576 + 3.565312) / 226.738272,
+    },
 }
 
 
@@ -145,20 +153,21 @@ def _code_digest(path):
     return hashlib.sha256("\n".join(lines).encode()).hexdigest()
 
 
-def _profiled_traffic(alg_bytes, kernel_id, workload_name):
+def _profiled_traffic(alg_bytes, kernel_id, workload_name, heads=None):
     """DRAM bytes of one launch scaled from the capture, or None once the
-    kernel source differs from the one profiled, for another kernel, or for
-    a workload other than the captured one (the DeepSeek-V3-shaped batch)."""
-    if kernel_id != 4 or workload_name != "dsv3":
+    kernel source differs from the one profiled, or for a kernel and
+    workload no capture covers."""
+    rec = PROFILED_TRAFFIC.get((kernel_id, workload_name, heads if workload_name == "fp8" else None))
+    if rec is None:
         return None
-    src = os.path.join(ROOT, "paged_mla_decode_06_gb300", "csrc", "decode_tc.cu")
+    src = os.path.join(ROOT, "paged_mla_decode_06_gb300", "csrc", rec["source"])
     try:
         digest = _code_digest(src)
     except OSError:
         return None
-    if digest != PROFILED_TRAFFIC["code_sha256"]:
+    if digest != rec["code_sha256"]:
         return None
-    return alg_bytes * PROFILED_TRAFFIC["dram_per_alg_byte"]
+    return alg_bytes * rec["dram_per_alg_byte"]
 
 
 def _alg_bytes_decode(w):
@@ -490,6 +499,7 @@ def side_workloads(B, dev, flush, stream, peaks, steps):
                     "kernel": int(plan.kernel), "rows_per_cta": int(plan.rows_per_cta),
                     "schedule": "balanced" if plan.schedule == 1 else "uniform",
                     "num_segments": int(plan.num_segments), "status_word": dw.status(),
+                    "traffic": _profiled_traffic(_alg_bytes_decode(w), int(plan.kernel), name, heads),
                     **roofline_of(w, dus, peaks)}
         del dw, dec_fn
         torch.cuda.empty_cache()
@@ -620,7 +630,7 @@ def run_gpu(args):
                     "unit": "TFLOP/s", "frac": rf["tensor_frac"],
                     "peak_source": f"bf16_tflops (burst) of {src}" +
                                    (" x 2 (nominal e4m3:bf16)" if w.kv_dtype == "fp8" else "")}
-        roof.update({"traffic": _profiled_traffic(alg, int(plan.kernel), args.workload),
+        roof.update({"traffic": _profiled_traffic(alg, int(plan.kernel), args.workload, args.heads),
                      "kernel": kname, "kernel_us": dms * 1e3, "algorithmic_bytes": alg,
                      "algorithmic_flops": rf["algorithmic_flops"],
                      "hbm_frac": rf["hbm_frac"], "tensor_tflops": rf["tensor_tflops"],
