@@ -39,12 +39,14 @@ __global__ void __launch_bounds__(kSeqThreads, 1) sparse_seqlen_kernel(
       indptr[t + 1] = static_cast<int>(visible < 0 ? 0 : (visible > topk ? topk : visible));
     }
   }
+  // tokens before the first request or past the last one get length 0
+  const int first = num_reqs > 0 ? max(qsl[0], 0) : 0;
   const int covered = num_reqs > 0 ? min(qsl[num_reqs], num_tokens) : 0;
   __syncthreads();  // pass 1's global writes are visible to the whole block
   int carry = 0;
   for (int t0 = 0; t0 < num_tokens; t0 += kSeqThreads) {
     const int t = t0 + tid;
-    const int len = t < covered ? indptr[t + 1] : 0;
+    const int len = t >= first && t < covered ? indptr[t + 1] : 0;
     int inc = len;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {

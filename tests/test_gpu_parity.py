@@ -582,6 +582,22 @@ def test_sparse_seqlen_bit_exact(topk):
     assert np.array_equal(ptr.cpu().numpy(), want_ptr)
 
 
+def test_sparse_seqlen_tokens_before_the_first_request():
+    # query_start_loc need not start at 0: the tokens before it have no list
+    qsl = np.array([3, 5, 9, 10], dtype=np.int32)
+    seq = np.array([4, 300, 2], dtype=np.int32)
+    want_lens, want_ptr = O.sparse_seqlen(qsl, seq, 128)
+    dev = torch.device("cuda")
+    lens = torch.full((10,), -7, dtype=torch.int32, device=dev)
+    ptr = torch.full((11,), -7, dtype=torch.int32, device=dev)
+    B.mla_sparse_seqlen(torch.from_numpy(qsl).to(dev), torch.from_numpy(seq).to(dev), topk=128,
+                        indptr=ptr, lens=lens)
+    torch.cuda.synchronize()
+    assert np.array_equal(lens.cpu().numpy(), want_lens)
+    assert np.array_equal(ptr.cpu().numpy(), want_ptr)
+    assert np.all(want_lens[:3] == 0)
+
+
 def test_sparse_seqlen_many_tokens():
     rng = np.random.default_rng(5)
     R = 3000
