@@ -530,7 +530,9 @@ def concat_quant_q(ql_nope, q_pe, q_scale=None):
                         np.asarray(q_pe, dtype=np.float64)], axis=-1)
     if q_scale is None:
         return q
-    # q / q_scale is taken in float32, the precision the kernel divides in, so
-    # both sides round the same quotient to e4m3.
+    # q / q_scale is formed in float32: the static per-tensor quantisation of
+    # forward_mqa (scaled_fp8_quant with the layer's float32 q scale) divides
+    # in the scale's type before rounding to e4m3, and a value on the edge
+    # between two codes must round the same way here.
     scaled = (q.astype(np.float32) / np.float32(q_scale)).astype(np.float64)
     return encode_e4m3fn(scaled)
