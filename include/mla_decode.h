@@ -66,7 +66,9 @@ typedef enum {
   MLA_ERR_INVALID_ARG = 1,   /* a shape, pointer, alignment or enum is invalid */
   MLA_ERR_UNSUPPORTED = 2,   /* valid but not built (e.g. head_dim != 576) */
   MLA_ERR_WORKSPACE = 3,     /* workspace missing or smaller than the plan needs */
-  MLA_ERR_CUDA = 4           /* a CUDA launch failed; see mla_last_cuda_error() */
+  MLA_ERR_CUDA = 4,          /* a CUDA launch failed; see mla_last_cuda_error() */
+  MLA_ERR_DEVICE_STATUS = 5  /* a kernel's bounded internal wait ran out: its status
+                                word in the workspace is set (mla_workspace_status) */
 } mla_status_t;
 
 typedef enum {
@@ -132,7 +134,12 @@ typedef struct {
                                   two per worker: 2 * (num_sms / 2) for the
                                   CTA-pair kernel, 2 * num_sms for the
                                   rows-as-N kernel */
-  int32_t reserved;
+  int32_t wait_limit_us;       /* bound on every internal wait of the tensor-core
+                                  kernels, in microseconds; the planner sets 0,
+                                  which means 2 s. A caller may lower it after
+                                  planning. A wait that runs out sets the
+                                  workspace status word and the kernel exits
+                                  without writing its outputs. */
   size_t workspace_bytes;      /* bytes mla_decode_fwd needs (>= 256) */
   size_t status_offset;        /* workspace layout, 256-B aligned pieces: a device */
   size_t segm_output_offset;   /* status word (int32) at offset 0, then, when */
@@ -203,9 +210,11 @@ MLA_API mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan
  *   workspace    plan->workspace_bytes of device memory, 256-byte aligned.
  *                Its first int32 is a device status word that must be zero
  *                before the first call (zero it once after allocating): the
- *                tensor-core kernel writes a nonzero code there, and leaves
- *                its outputs unwritten, if one of its bounded internal waits
- *                times out. The rest needs no initialisation.
+ *                tensor-core kernels write a nonzero code there, and leave
+ *                their outputs unwritten, if one of their bounded internal
+ *                waits runs out (plan->wait_limit_us; read it, and reset it,
+ *                with mla_workspace_status). The rest needs no
+ *                initialisation.
  *   out          [T, H, 512] bf16; lse [T, H] fp32 natural log. Every element
  *                is written; a row with no visible key gets out = 0 and
  *                lse = -inf (or its sink).
@@ -311,7 +320,8 @@ MLA_API mla_status_t mla_merge_segments(const float* segm_output, const float* s
  * query_start_loc[r] tokens) sees its causal prefix (the bound of [dense]
  * dcp_local_verify_row_lens) and selects at most topk positions:
  *   lens[t] = clamp(seq_lens[r] - qlen + j + 1, 0, topk).
- * Tokens at or past query_start_loc[num_reqs] get length 0.
+ * Tokens before query_start_loc[0] or at or past query_start_loc[num_reqs]
+ * get length 0.
  *   query_start_loc [num_reqs + 1] int32, nondecreasing; seq_lens [num_reqs]
  *   lens [num_tokens] int32 or NULL; indptr [num_tokens + 1] int32
  * One block on `stream`. Errors: MLA_ERR_INVALID_ARG for negative sizes,
@@ -427,7 +437,11 @@ MLA_API mla_status_t mla_concat_quant_q(const void* ql_nope, int64_t nope_stride
  *     any stream capture begins.
  *   - Size limit: a plan whose workspace_bytes exceeds
  *     MLA_STATIC_SCRATCH_BYTES is rejected with MLA_ERR_WORKSPACE before any
- *     device work. NS == 1 plans (prob.num_segments = 1) need only 256 bytes.
+ *     device work. Only plans requested with prob.num_segments = 1 are sure
+ *     to fit (they need 256 bytes); a planner-chosen balanced plan needs its
+ *     work list and partial slots (about 41 MB for 64 requests of 128 heads on
+ *     a 152-SM part) and, for very many requests, can exceed the limit and
+ *     is then refused.
  *   - Sharing: every call on a device uses the same array, which keeps the
  *     last call's partials. Each call first clears the array's status word
  *     (stream-ordered memset); nothing else must start at zero. Calls whose
@@ -446,6 +460,21 @@ MLA_API mla_status_t mla_decode_fwd_static(const mla_plan_t* plan, const void* q
                                            float q_scale, float kv_scale, const float* sinks,
                                            void* out, float* lse, int32_t* status_out,
                                            cudaStream_t stream);
+
+/*
+ * mla_workspace_status -- the device status word of a workspace, after the
+ * work enqueued on `stream` so far (the stream is synchronised: call it
+ * between steps, not inside a captured graph). The tensor-core decode
+ * kernels write a nonzero code there, and leave their outputs unwritten,
+ * when one of their bounded internal waits runs out (plan->wait_limit_us);
+ * nothing else writes it. *code receives the word; with clear != 0 a nonzero
+ * word is reset to 0 (stream-ordered), so that the workspace can serve the
+ * next call.
+ * Returns MLA_OK when the word was 0, MLA_ERR_DEVICE_STATUS when it was not,
+ * MLA_ERR_INVALID_ARG for NULL or misaligned pointers, MLA_ERR_CUDA.
+ */
+MLA_API mla_status_t mla_workspace_status(const mla_plan_t* plan, const void* workspace,
+                                          int32_t* code, int32_t clear, cudaStream_t stream);
 
 /* Human-readable name of a status code (static storage). */
 MLA_API const char* mla_status_string(mla_status_t status);

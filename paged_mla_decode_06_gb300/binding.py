@@ -18,6 +18,7 @@ MLA_ERR_INVALID_ARG = 1
 MLA_ERR_UNSUPPORTED = 2
 MLA_ERR_WORKSPACE = 3
 MLA_ERR_CUDA = 4
+MLA_ERR_DEVICE_STATUS = 5
 
 MLA_DTYPE_BF16 = 0
 MLA_DTYPE_FP8_E4M3 = 1
@@ -51,7 +52,7 @@ class Problem(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [("prob", Problem)] + [(n, ctypes.c_int32) for n in (
         "num_segments", "tile_size", "kernel", "rows_per_cta", "row_tiles", "grid_x", "grid_y",
-        "grid_z", "num_sms", "schedule", "max_items", "split_items", "reserved")] + [
+        "grid_z", "num_sms", "schedule", "max_items", "split_items", "wait_limit_us")] + [
         ("workspace_bytes", ctypes.c_size_t), ("status_offset", ctypes.c_size_t),
         ("segm_output_offset", ctypes.c_size_t), ("segm_max_offset", ctypes.c_size_t),
         ("segm_expsum_offset", ctypes.c_size_t)]
@@ -121,6 +122,9 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
                                            ctypes.c_int32, ctypes.c_int32, ctypes.c_float, _vp,
                                            _vp]
         lib.mla_concat_quant_q.restype = st
+        lib.mla_workspace_status.argtypes = [ctypes.POINTER(Plan), _vp, ctypes.POINTER(ctypes.c_int32),
+                                             ctypes.c_int32, _vp]
+        lib.mla_workspace_status.restype = st
         lib.mla_status_string.argtypes = [ctypes.c_int32]
         lib.mla_status_string.restype = ctypes.c_char_p
         lib.mla_last_cuda_error.argtypes = []
@@ -133,7 +137,7 @@ def load_library(path: str | None = None) -> ctypes.CDLL:
 
 def _status_name(status: int) -> str:
     names = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
-             3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA"}
+             3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE_STATUS"}
     return names.get(int(status), f"status {status}")
 
 
@@ -218,6 +222,19 @@ def mla_decode_fwd_static(plan: Plan, q, kv_cache, *, block_table=None,
         _ptr(seq_lens), _ptr(qo_indptr), _ptr(sparse_slots), _ptr(sparse_indptr),
         float(softmax_scale), float(q_scale), float(kv_scale), _ptr(sinks), _ptr(out), _ptr(lse),
         _ptr(status_out), _stream(stream)))
+
+
+def mla_workspace_status(plan: Plan, workspace, *, clear: bool = False, stream=None) -> int:
+    """The workspace's device status word after the stream's work so far
+    (0: no kernel reported a timed-out wait); with ``clear`` a nonzero word
+    is reset. Returns the word instead of raising on MLA_ERR_DEVICE_STATUS."""
+    lib = load_library()
+    code = ctypes.c_int32(0)
+    st = lib.mla_workspace_status(ctypes.byref(plan), _ptr(workspace), ctypes.byref(code),
+                                  1 if clear else 0, _stream(stream))
+    if st not in (MLA_OK, MLA_ERR_DEVICE_STATUS):
+        _check("mla_workspace_status", st)
+    return int(code.value)
 
 
 def _ws_bytes(workspace) -> int:

@@ -123,6 +123,7 @@ mla::DecodeParams make_params(const mla_plan_t* plan, const Inputs& in) {
   d.row_tiles = plan->row_tiles;
   d.score_scale_log2 = in.softmax_scale * in.q_scale * in.kv_scale * 1.4426950408889634f;
   d.kv_scale = in.kv_scale;
+  d.wait_ns = plan->wait_limit_us > 0 ? static_cast<uint64_t>(plan->wait_limit_us) * 1000ull : 0ull;
   return d;
 }
 
@@ -278,6 +279,7 @@ const char* mla_status_string(mla_status_t s) {
     case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
     case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
     case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+    case MLA_ERR_DEVICE_STATUS: return "MLA_ERR_DEVICE_STATUS";
     default: return "MLA_ERR_UNKNOWN";
   }
 }
@@ -472,6 +474,20 @@ mla_status_t mla_decode_fwd(const mla_plan_t* plan, const void* q, const void* k
   m.out = out;
   m.lse = lse;
   return cuda_status(mla::launch_merge(m, stream));
+}
+
+mla_status_t mla_workspace_status(const mla_plan_t* plan, const void* workspace, int32_t* code,
+                                  int32_t clear, cudaStream_t stream) {
+  if (plan == nullptr || workspace == nullptr || code == nullptr) return MLA_ERR_INVALID_ARG;
+  if (!aligned(workspace, kWsAlign) || !aligned(code, 4)) return MLA_ERR_INVALID_ARG;
+  uint8_t* word = static_cast<uint8_t*>(const_cast<void*>(workspace)) + plan->status_offset;
+  int32_t v = 0;
+  cudaError_t e = cudaMemcpyAsync(&v, word, sizeof(v), cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e == cudaSuccess && clear != 0 && v != 0) e = cudaMemsetAsync(word, 0, sizeof(v), stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  *code = v;
+  return v == 0 ? MLA_OK : MLA_ERR_DEVICE_STATUS;
 }
 
 mla_status_t mla_decode_schedule(const mla_plan_t* plan, const int32_t* seq_lens,

@@ -157,7 +157,8 @@ constexpr uint32_t kSleepNs = 20000;
 __device__ bool wait_phase(const Ctx& x, uint32_t bar, uint32_t parity, int code) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait_sleep(bar, parity, kSleepNs)) {
+  const uint32_t nap = x.limit_ns < kSleepNs ? static_cast<uint32_t>(x.limit_ns) : kSleepNs;
+  while (!mbar_try_wait_sleep(bar, parity, nap)) {
     if (*x.abort) return false;
     if (global_timer_ns() - t0 > x.limit_ns) {
       report(x.status, code);

@@ -130,6 +130,7 @@ struct Ctx {
   uint32_t peer;        // shared::cluster address of the peer's shared-memory base
   volatile int* abort;
   int* status;
+  uint64_t limit_ns;    // bound on each wait (drains keep kTimeoutNs)
   uint32_t tbase;
   int tid, warp, lane;
   int H, tok0, qlen, row0, rows_total, part_len;
@@ -149,11 +150,12 @@ struct Ctx {
 __device__ bool wait_phase(const Ctx& x, uint32_t bar, uint32_t parity, bool cluster, int code) {
   if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
+  const uint32_t nap = x.limit_ns < 20000u ? static_cast<uint32_t>(x.limit_ns) : 20000u;
   for (;;) {
-    const bool ok = cluster ? mbar_try_wait_cluster_sleep(bar, parity, 20000u) : mbar_try_wait_sleep(bar, parity, 20000u);
+    const bool ok = cluster ? mbar_try_wait_cluster_sleep(bar, parity, nap) : mbar_try_wait_sleep(bar, parity, nap);
     if (ok) return true;
     if (*x.abort) return false;
-    if (global_timer_ns() - t0 > kTimeoutNs) {
+    if (global_timer_ns() - t0 > x.limit_ns) {
       report(x.status, code);
       *x.abort = 1;
       return false;
@@ -883,6 +885,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
   Ctx x;
   x.smem = smem;
   x.status = status;
+  x.limit_ns = p.wait_ns != 0 ? p.wait_ns : kTimeoutNs;
   x.tid = threadIdx.x;
   x.warp = x.tid >> 5;
   x.lane = x.tid & 31;

@@ -49,7 +49,7 @@ def test_struct_sizes_match_the_header(lib):
 
 def test_status_strings(lib):
     for code, name in [(0, "MLA_OK"), (1, "MLA_ERR_INVALID_ARG"), (2, "MLA_ERR_UNSUPPORTED"),
-                       (3, "MLA_ERR_WORKSPACE"), (4, "MLA_ERR_CUDA")]:
+                       (3, "MLA_ERR_WORKSPACE"), (4, "MLA_ERR_CUDA"), (5, "MLA_ERR_DEVICE_STATUS")]:
         assert lib.mla_status_string(code).decode() == name
     assert lib.mla_version() >= 100
 
@@ -391,3 +391,15 @@ def test_plan_random_problems_are_consistent(lib):
                              num_segments=int(rng.choice([-1, 65])))
         out = B.Plan()
         assert lib.mla_decode_plan(ctypes.byref(bad), ctypes.byref(out)) == B.MLA_ERR_INVALID_ARG
+
+
+def test_workspace_status_rejects_bad_arguments(lib):
+    plan = B.mla_decode_plan(_dense_problem())
+    assert plan.wait_limit_us == 0  # the planner leaves the default (2 s)
+    code = ctypes.c_int32(7)
+    f = lib.mla_workspace_status
+    assert f(None, FAKE, ctypes.byref(code), 0, None) == B.MLA_ERR_INVALID_ARG
+    assert f(ctypes.byref(plan), None, ctypes.byref(code), 0, None) == B.MLA_ERR_INVALID_ARG
+    assert f(ctypes.byref(plan), FAKE, None, 0, None) == B.MLA_ERR_INVALID_ARG
+    assert f(ctypes.byref(plan), FAKE + 64, ctypes.byref(code), 0, None) == B.MLA_ERR_INVALID_ARG
+    assert code.value == 7  # nothing written on a refused call
