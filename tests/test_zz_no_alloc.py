@@ -1,7 +1,9 @@
 """mla_decode_fwd_static: the decode on the library's file-scope device scratch
-(no caller workspace) agrees with mla_decode_fwd on the same inputs, over two
-calls in a row on different workloads, and rejects plans larger than the
-scratch before touching the device.
+(no caller workspace) agrees with mla_decode_fwd on the same inputs and with
+the fp64 oracle on sampled tokens, over calls in a row on different
+workloads and partitions (uniform split-K, and the balanced schedule, whose
+work list and partial slots are the largest use of the scratch), and
+rejects plans larger than the scratch before touching the device.
 
 Collected last on purpose: it must hold both alone in a fresh process and
 after every other test has run in the same process.
@@ -32,14 +34,17 @@ def test_static_rejects_plans_beyond_the_scratch():
     assert lib.mla_status_string(st).decode() == "MLA_ERR_WORKSPACE"
 
 
-def _static_vs_fwd(w, num_segments):
+def _static_vs_fwd(w, num_segments, tokens):
     import torch
 
-    from tests.gpu_helpers import TOL_LSE, TOL_OUT
+    from tests.gpu_helpers import TOL_LSE, TOL_OUT, assert_close, run_oracle
 
     dw = B.DeviceWorkload(w, num_segments=num_segments)
     assert 0 < dw.plan.workspace_bytes <= STATIC_SCRATCH_BYTES
-    assert dw.plan.num_segments > 1  # the partials live in the scratch
+    if num_segments:
+        assert dw.plan.num_segments > 1  # the partials live in the scratch
+    else:
+        assert dw.plan.schedule == 1     # work list, unit table and partial slots in the scratch
     if w.sparse:
         dw.convert()
     dw.forward(convert=False)
@@ -68,13 +73,25 @@ def _static_vs_fwd(w, num_segments):
     assert np.array_equal(np.isneginf(got_lse), ninf)
     lerr = float(np.max(np.abs(got_lse[~ninf] - ref_lse[~ninf]))) if (~ninf).any() else 0.0
     assert lerr <= TOL_LSE, f"{w.name}: max |static lse - fwd lse| = {lerr:.3e}"
+    # and against the fp64 oracle on sampled tokens
+    or_o, or_l = run_oracle(w, tokens=tokens)
+    assert_close(got_out[tokens], got_lse[tokens], or_o, or_l, w.kv_dtype, f"{w.name} static vs oracle")
 
 
 @pytest.mark.gpu
-def test_static_matches_fwd_on_two_calls_in_a_row():
+def test_static_matches_fwd_on_calls_in_a_row():
     BUILD.build()
     # first call: DeepSeek-V3-shaped bf16 decode, 4 segments
-    _static_vs_fwd(I.dsv3_bf16(seed=21, batch=8, seq_lo=700, seq_hi=5000), num_segments=4)
+    _static_vs_fwd(I.dsv3_bf16(seed=21, batch=8, seq_lo=700, seq_hi=5000), num_segments=4,
+                   tokens=[0, 7])
     # second call, same scratch: multi-token rows with sinks, 3 segments,
     # a different partial layout than the first call left behind
-    _static_vs_fwd(I.mtp_sinks(seed=22, batch=4, median=2000.0, hi=6000), num_segments=3)
+    _static_vs_fwd(I.mtp_sinks(seed=22, batch=4, median=2000.0, hi=6000), num_segments=3,
+                   tokens=[0, 5])
+    # third: the planner's default for 128 heads, the balanced schedule on the
+    # CTA-pair kernel (~41 MB of work list and partial slots)
+    _static_vs_fwd(I.dsv3_bf16(seed=23, batch=64, seq_lo=1024, seq_hi=8192), num_segments=0,
+                   tokens=[0, 31, 63])
+    # fourth: e4m3 at 16 heads, the balanced schedule on the rows-as-N kernel
+    _static_vs_fwd(I.fp8_decode(16, seed=24, batch=12, seq_len=8192), num_segments=0,
+                   tokens=[0, 11])
