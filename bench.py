@@ -715,10 +715,11 @@ def run_reference(args):
 
 def run_kernels_once():
     """One launch of every library kernel on inputs above the 129 MB L2, for
-    a profiler's counter pass (no timing, no JSON line): the e4m3 decode
-    (schedule, tensor-core decode, merge), the sparse decode (index
-    conversion, schedule, decode, merge), the warp-MMA decode (decode,
-    merge), the q concat/quantisation, the per-shard LSE merge, the sparse
+    a profiler's counter pass (no timing, no JSON line): the e4m3 decode at
+    128 heads (schedule, CTA-pair decode, merge), the sparse decode (index
+    conversion, schedule, decode, merge), the e4m3 decode at 16 heads on the
+    warp-MMA kernel and on the rows-as-N kernel, the multi-token decode with
+    sinks, the q concat/quantisation, the per-shard LSE merge, the sparse
     list lengths and the fixed-width fit."""
     import torch
     from paged_mla_decode_06_gb300 import binding as B
@@ -730,9 +731,12 @@ def run_kernels_once():
     wf = I.fp8_decode(128, batch=16)                    # 16 x 16384 x 576 B = 151 MB
     ws = I.sparse_topk(num_reqs=8, cache_tokens=32768)  # 64 tokens x 2048 rows x 1152 B
     wm = I.fp8_decode(16, batch=16)
+    wt = I.mtp_sinks(batch=16)                          # multi-token rows: 2-4 row tiles per request
     dwf = B.DeviceWorkload(wf, device=dev)
     dws = B.DeviceWorkload(ws, device=dev)
     dwm = B.DeviceWorkload(wm, device=dev, kernel=B.MLA_KERNEL_WARP_MMA)
+    dwn = B.DeviceWorkload(wm, device=dev)              # the rows-as-N kernel on the same batch
+    dwt = B.DeviceWorkload(wt, device=dev)
     g = torch.Generator(device=dev).manual_seed(11)
     T, H = 1024, 128
     nope = torch.randn(T, H, 512, device=dev, generator=g).to(torch.bfloat16)
@@ -752,12 +756,14 @@ def run_kernels_once():
     dwf.forward()
     dws.forward()
     dwm.forward()
+    dwn.forward()
+    dwt.forward()
     B.mla_concat_quant_q(nope, pe, out=qout, q_scale=0.05)
     B.mla_merge_lse(sh_out, sh_lse, out=mo, lse=ml)
     B.mla_sparse_seqlen(qsl, seq, topk=2048, indptr=ptr)
     B.mla_fit_kpool_indices(ti, topk=2048, out=fit)
     torch.cuda.synchronize()
-    if dwf.status() != 0 or dws.status() != 0:
+    if any(d.status() != 0 for d in (dwf, dws, dwn, dwt)):
         raise RuntimeError("device status word set")
     print("kernels-once ok")
 
