@@ -16,6 +16,7 @@ constexpr int kRank = 512;
 constexpr int kMaxHeads = 128;
 constexpr int kMaxSegments = 64;
 constexpr int kSparseTile = 64;
+constexpr int64_t kRowsNMax = 128;  // query rows per request the rows-as-N kernel takes (2 tiles)
 constexpr size_t kWsAlign = 256;
 
 thread_local const char* g_last_cuda_error = "";
@@ -312,7 +313,7 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   // the rows-as-N kernel: e4m3 dense (block size a multiple of 64), at most 64 rows
   const bool tc_ok = sparse ? p.kv_dtype == MLA_DTYPE_BF16 : p.block_size % 64 == 0;
   const bool rn_ok = !sparse && p.kv_dtype == MLA_DTYPE_FP8_E4M3 && p.block_size % 64 == 0 &&
-                     rows_per_unit <= 64;
+                     rows_per_unit <= kRowsNMax;
   if (p.kernel == MLA_KERNEL_TCGEN05 && !tc_ok) return MLA_ERR_UNSUPPORTED;
   if (p.kernel == MLA_KERNEL_TCGEN05_ROWS_N && !rn_ok) return MLA_ERR_UNSUPPORTED;
   const bool use_rn = p.kernel == MLA_KERNEL_TCGEN05_ROWS_N || (p.kernel == MLA_KERNEL_AUTO && rn_ok);
@@ -320,8 +321,12 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   const bool use_tc = use_rn || use_pair;
   int32_t kernel, rows;
   if (use_rn) {
+    // up to 64 rows per CTA; more rows take several tiles of equal size,
+    // each a CTA of its own over the request's keys (the tiles of a request
+    // run side by side, so that all but the first read the KV from L2)
     kernel = mla::kTcRowsN;
-    rows = static_cast<int32_t>((rows_per_unit + 15) / 16 * 16);
+    const int64_t tiles = (rows_per_unit + 63) / 64;
+    rows = static_cast<int32_t>(((rows_per_unit + tiles - 1) / tiles + 15) / 16 * 16);
   } else if (use_pair) {
     kernel = mla::kTcPair128;
     rows = 128;

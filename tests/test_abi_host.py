@@ -119,7 +119,8 @@ def test_plan_sparse(lib):
     (dict(mixed_dtype=True), B.MLA_ERR_UNSUPPORTED),
     (dict(kernel=2, block_size=16, max_blocks_per_req=600), B.MLA_ERR_UNSUPPORTED),
     (dict(kernel=3), B.MLA_ERR_UNSUPPORTED),              # rows-as-N: e4m3 only
-    (dict(kernel=3, dtype="fp8"), B.MLA_ERR_UNSUPPORTED), # rows-as-N: 128 heads > 64 rows
+    (dict(kernel=3, dtype="fp8", num_tokens=128, max_qlen=2),
+     B.MLA_ERR_UNSUPPORTED),                              # rows-as-N: 256 rows > 128
     (dict(kernel=3, dtype="fp8", num_heads=16, block_size=16, max_blocks_per_req=600),
      B.MLA_ERR_UNSUPPORTED),                              # rows-as-N: block size not 64k
     (dict(kernel=4), B.MLA_ERR_INVALID_ARG),
@@ -277,7 +278,10 @@ def test_plan_rows_as_n(lib, heads, qlen, rows):
     # the CTA pair and the warp-MMA kernel can still be asked for
     assert B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=heads, num_tokens=64 * qlen,
                                             max_qlen=qlen, kernel=B.MLA_KERNEL_TCGEN05)).kernel == 4
-    wide = B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=65))
+    # 65-128 rows: two row tiles of equal size; more rows go to the CTA pair
+    two = B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=96))
+    assert two.kernel == 5 and two.row_tiles == 2 and two.rows_per_cta == 48
+    wide = B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=128, num_tokens=128, max_qlen=2))
     assert wide.kernel == 4
 
 
@@ -365,10 +369,12 @@ def test_plan_random_problems_are_consistent(lib):
         assert plan.grid_x >= 1 and plan.grid_y >= 1 and plan.grid_z == units
         assert plan.workspace_bytes >= 256 and plan.workspace_bytes % 256 == 0
         rn_ok = (not sparse and prob.kv_dtype == B.MLA_DTYPE_FP8_E4M3 and bs % 64 == 0
-                 and heads * prob.max_qlen <= 64)
+                 and heads * prob.max_qlen <= 128)
         if rn_ok:  # the planner's first choice wherever it can run
-            assert plan.kernel == 5 and plan.rows_per_cta == -(-heads * prob.max_qlen // 16) * 16
-            assert plan.row_tiles == 1 and plan.grid_x == 1
+            rows = heads * prob.max_qlen
+            tiles = -(-rows // 64)
+            assert plan.kernel == 5 and plan.row_tiles == tiles and plan.grid_x == tiles
+            assert plan.rows_per_cta == -(-(-(-rows // tiles)) // 16) * 16
         if plan.schedule == 1:
             assert plan.kernel in (4, 5) and ns == 0 and plan.num_segments == 1
             workers = max(1, sms // 2) if plan.kernel == 4 else sms

@@ -503,15 +503,18 @@ def test_full_dsv3_bf16_sampled(kernel):
                  f"full dsv3 ns={dw.plan.num_segments} k={kernel}")
 
 
+@pytest.mark.parametrize("kernel", [B.MLA_KERNEL_AUTO, B.MLA_KERNEL_TCGEN05], ids=["auto", "pair"])
 @pytest.mark.parametrize("heads", [96, 128])
-def test_fp8_planner_path_split_rows(heads):
-    # e4m3 above 64 heads: the planner's default is the CTA pair under the
-    # balanced schedule; 6 requests x 4096 keys on 76 pairs split every row
+def test_fp8_planner_path_split_rows(heads, kernel):
+    # e4m3 above 64 heads under the balanced schedule: the planner's default
+    # (the rows-as-N kernel, two row tiles per request) and the CTA pair;
+    # 6 requests x 4096 keys on 76-152 workers split every row
     w = I.fp8_decode(heads, batch=6, seq_len=4096, num_segments=0)
-    out, lse, dw = run_gpu(w)
-    assert dw.plan.kernel == 4 and dw.plan.schedule == 1
+    out, lse, dw = run_gpu(w, kernel=kernel)
+    assert dw.plan.schedule == 1
+    assert dw.plan.kernel == (5 if kernel == B.MLA_KERNEL_AUTO else 4)
     ref_o, ref_l = run_oracle(w)
-    assert_close(out, lse, ref_o, ref_l, "fp8", f"fp8 planner path H={heads}")
+    assert_close(out, lse, ref_o, ref_l, "fp8", f"fp8 planner path H={heads} kernel={dw.plan.kernel}")
 
 
 @pytest.mark.parametrize("heads", [16, 128])
