@@ -111,9 +111,11 @@ typedef enum {
                                   or e4m3 with block_size a multiple of 64, or
                                   sparse bf16 */
   MLA_KERNEL_TCGEN05_ROWS_N = 3 /* tcgen05/TMEM kernel with the query rows as
-                                  the MMA N dimension, one CTA per 16..64 rows:
+                                  the MMA N dimension, one CTA per 16..64 rows
+                                  (a cluster of two CTAs sharing each key box
+                                  for 65..128 rows):
                                   dense e4m3 with block_size a multiple of 64
-                                  and num_heads * max_qlen <= 64 */
+                                  and num_heads * max_qlen <= 128 */
 } mla_kernel_t;
 
 /* Filled by mla_decode_plan; pass it unchanged to mla_decode_fwd or
@@ -124,22 +126,27 @@ typedef struct {
   int32_t tile_size;           /* partition unit: tiles_per_segment =
                                   cdiv(len, NS * tile_size) ([merge] docstring) */
   int32_t kernel;              /* decode kernel variant (internal id) */
-  int32_t rows_per_cta;        /* query rows (token x head) one CTA owns */
+  int32_t rows_per_cta;        /* query rows (token x head) one CTA owns (the
+                                  CTA-pair kernel: one pair) */
   int32_t row_tiles;           /* row tiles per request (dense) or token (sparse) */
   int32_t grid_x, grid_y, grid_z;
   int32_t num_sms;
   int32_t schedule;            /* 1: balanced schedule (see mla_decode_plan), else 0 */
   int32_t max_items;           /* balanced: work items the decode grid holds */
-  int32_t split_items;         /* balanced: partial slots of rows_per_cta rows,
+  int32_t split_items;         /* balanced: partial slots of tile_rows rows,
                                   two per worker: 2 * (num_sms / 2) for the
                                   CTA-pair kernel, 2 * num_sms for the
-                                  rows-as-N kernel */
+                                  rows-as-N kernel (2 * the clusters of two
+                                  that fit at once, for 65..128 rows) */
   int32_t wait_limit_us;       /* bound on every internal wait of the tensor-core
                                   kernels, in microseconds; the planner sets 0,
                                   which means 2 s. A caller may lower it after
                                   planning. A wait that runs out sets the
                                   workspace status word and the kernel exits
                                   without writing its outputs. */
+  int32_t tile_rows;           /* query rows of a row tile: rows_per_cta times
+                                  the CTAs that share the tile's keys (1 or 2),
+                                  or 128 for the CTA-pair kernel */
   size_t workspace_bytes;      /* bytes mla_decode_fwd needs (>= 256) */
   size_t status_offset;        /* workspace layout, 256-B aligned pieces: a device */
   size_t segm_output_offset;   /* status word (int32) at offset 0, then, when */
@@ -160,19 +167,22 @@ typedef struct {
  * sizes the segments on the device from the lengths of the call (the work
  * list of [sparse] _forward_mla's persistent path, work_indptr /
  * reduce_indptr / reduce_partial_map). Rows (a unit, i.e. a dense request or
- * a sparse token, times its tiles of rows_per_cta query rows) of
+ * a sparse token, times its tiles of tile_rows query rows) of
  * g = cdiv(len, 128) key groups are laid end to end and the sequence of all
- * groups is cut every W = cdiv(total, workers) groups (workers: num_sms / 2
- * CTA pairs, or num_sms CTAs for the rows-as-N kernel), cuts within W / 8 of
- * a row's ends dropped; the pieces run longest first (max_items = rows +
- * workers). Unsplit rows are written by the decode kernel itself; split rows
- * write base-2 partials to slots of rows_per_cta rows in the workspace
- * (split_items = 2 * workers of them) and mla_merge_items combines them.
- * Workspace layout: status block, item count at 256, items (32 bytes each,
- * max_items of them) at 512, the unit table (int32 pairs {first slot or -1,
- * pieces} per unit and row tile) at the next 256-byte boundary, then
- * segm_output [split_items * rows_per_cta, 512], segm_max and segm_expsum
- * [split_items * rows_per_cta] at the plan's offsets.
+ * groups is cut every W = cdiv(total, workers) groups. CTA-pair kernel:
+ * workers = num_sms / 2 pairs, cuts within W / 8 of a row's ends dropped,
+ * one item per pair, the pieces longest first. Rows-as-N kernel: workers =
+ * num_sms CTAs (or the clusters of two that fit), every cut kept, and
+ * worker w runs the pieces of groups [w W, (w + 1) W) one after another.
+ * max_items = rows + workers. Unsplit rows are written by the decode kernel
+ * itself; split rows write base-2 partials to slots of tile_rows rows in the
+ * workspace (split_items = 2 * workers of them) and mla_merge_items combines
+ * them. Workspace layout: status block, item count at 256, items (32 bytes
+ * each, max_items of them) at 512, the unit table (int32 pairs {first slot
+ * or -1, pieces} per unit and row tile) at the next 256-byte boundary, each
+ * worker's first item (int32, workers + 1) at the next, then segm_output
+ * [split_items * tile_rows, 512], segm_max and segm_expsum
+ * [split_items * tile_rows] at the plan's offsets.
  * Errors: MLA_ERR_INVALID_ARG for NULL pointers or inconsistent sizes,
  * MLA_ERR_UNSUPPORTED for head_dim != 576, kv_lora_rank != 512,
  * num_heads > 128, q_dtype != kv_dtype, or topk not a multiple of 128.

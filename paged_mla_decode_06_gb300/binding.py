@@ -52,7 +52,7 @@ class Problem(ctypes.Structure):
 class Plan(ctypes.Structure):
     _fields_ = [("prob", Problem)] + [(n, ctypes.c_int32) for n in (
         "num_segments", "tile_size", "kernel", "rows_per_cta", "row_tiles", "grid_x", "grid_y",
-        "grid_z", "num_sms", "schedule", "max_items", "split_items", "wait_limit_us")] + [
+        "grid_z", "num_sms", "schedule", "max_items", "split_items", "wait_limit_us", "tile_rows")] + [
         ("workspace_bytes", ctypes.c_size_t), ("status_offset", ctypes.c_size_t),
         ("segm_output_offset", ctypes.c_size_t), ("segm_max_offset", ctypes.c_size_t),
         ("segm_expsum_offset", ctypes.c_size_t)]

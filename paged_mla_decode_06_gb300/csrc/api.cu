@@ -16,7 +16,10 @@ constexpr int kRank = 512;
 constexpr int kMaxHeads = 128;
 constexpr int kMaxSegments = 64;
 constexpr int kSparseTile = 64;
-constexpr int64_t kRowsNMax = 128;  // query rows per request the rows-as-N kernel takes (2 tiles)
+constexpr int64_t kRowsNMax = 128;  // query rows per request the rows-as-N kernel takes (a CTA pair)
+constexpr int32_t kMaxWorkers = 1024;  // workers of the contiguous schedule
+static_assert(sizeof(mla_problem_t) == 68 && sizeof(mla_plan_t) == 168,
+              "the plan layout the bindings mirror");
 constexpr size_t kWsAlign = 256;
 
 thread_local const char* g_last_cuda_error = "";
@@ -154,10 +157,11 @@ dim3 grid_of(const mla_plan_t* plan) {
 }
 
 // Workspace pieces of the balanced schedule (after the status block):
-// the item count, the items (32 bytes each), the unit table, then the
-// partial slots at the plan's segm_* offsets.
+// the item count, the items (32 bytes each), the unit table, each worker's
+// first item (rows-as-N kernel), then the partial slots at the plan's
+// segm_* offsets.
 struct SchedLayout {
-  size_t n_items, items, unit_tab, end;
+  size_t n_items, items, unit_tab, worker_first, end;
 };
 
 SchedLayout sched_layout(const mla_plan_t* plan) {
@@ -167,11 +171,13 @@ SchedLayout sched_layout(const mla_plan_t* plan) {
   l.n_items = kWsAlign;
   l.items = 2 * kWsAlign;
   l.unit_tab = l.items + align_up(static_cast<size_t>(plan->max_items) * 32, kWsAlign);
-  l.end = l.unit_tab + align_up(units * static_cast<size_t>(plan->row_tiles) * 8, kWsAlign);
+  l.worker_first = l.unit_tab + align_up(units * static_cast<size_t>(plan->row_tiles) * 8, kWsAlign);
+  l.end = l.worker_first + align_up((static_cast<size_t>(plan->split_items) / 2 + 1) * 4, kWsAlign);
   return l;
 }
 
-// d.items selects the balanced grid: one CTA pair (or CTA) per item slot.
+// d.items selects the balanced grid: one CTA pair per item slot (CTA-pair
+// kernel), one CTA or cluster per worker (rows-as-N kernel).
 mla_status_t launch_decode(const mla_plan_t* plan, const mla::DecodeParams& d, int* status,
                            cudaStream_t stream) {
   if (plan->grid_z == 0) return MLA_OK;
@@ -185,9 +191,11 @@ mla_status_t launch_decode(const mla_plan_t* plan, const mla::DecodeParams& d, i
                                              grid, status, stream));
   }
   if (plan->kernel == mla::kTcRowsN) {
-    const dim3 grid = d.items != nullptr ? dim3(items, 1u, 1u) : grid_of(plan);
-    return cuda_status(mla::launch_decode_hn(d, plan->rows_per_cta, q_rows, kv_rows, grid, status,
-                                             stream));
+    const int cluster = plan->tile_rows / plan->rows_per_cta;
+    const unsigned workers = static_cast<unsigned>(plan->split_items / 2);
+    const dim3 grid = d.items != nullptr ? dim3(workers * cluster, 1u, 1u) : grid_of(plan);
+    return cuda_status(mla::launch_decode_hn(d, plan->rows_per_cta, cluster, q_rows, kv_rows, grid,
+                                             status, stream));
   }
   return cuda_status(mla::launch_decode_mma(plan->kernel, p.kv_dtype == MLA_DTYPE_FP8_E4M3, d,
                                             grid_of(plan), stream));
@@ -207,18 +215,23 @@ mla::SchedParams sched_params(const mla_plan_t* plan, const Inputs& in, uint8_t*
   sp.num_units = p.topk > 0 ? p.num_tokens : p.num_reqs;
   sp.num_heads = p.num_heads;
   sp.tiles_max = plan->row_tiles;
-  sp.tile_rows = plan->rows_per_cta;
+  sp.tile_rows = plan->tile_rows;
   sp.split_cap = plan->split_items;
   sp.items = reinterpret_cast<int32_t*>(ws + l.items);
   sp.n_items = reinterpret_cast<int32_t*>(ws + l.n_items);
   sp.unit_tab = reinterpret_cast<int32_t*>(ws + l.unit_tab);
+  if (plan->kernel == mla::kTcRowsN) {  // workers run contiguous runs of items
+    sp.worker_first = reinterpret_cast<int32_t*>(ws + l.worker_first);
+    sp.workers = plan->split_items / 2;
+  }
   return sp;
 }
 
 mla_status_t check_scheduled(const mla_plan_t* plan, const void* workspace, size_t workspace_bytes) {
   if (plan == nullptr || plan->schedule != 1) return MLA_ERR_INVALID_ARG;
   if ((plan->kernel != mla::kTcPair128 && plan->kernel != mla::kTcRowsN) || plan->max_items <= 0 ||
-      plan->split_items <= 0 || plan->row_tiles <= 0 || plan->rows_per_cta <= 0)
+      plan->split_items <= 0 || plan->row_tiles <= 0 || plan->rows_per_cta <= 0 ||
+      plan->tile_rows < plan->rows_per_cta || plan->split_items / 2 > kMaxWorkers)
     return MLA_ERR_INVALID_ARG;
   if (workspace == nullptr || workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE;
   if (!aligned(workspace, kWsAlign)) return MLA_ERR_INVALID_ARG;
@@ -235,11 +248,13 @@ mla_status_t run_items(const mla_plan_t* plan, const Inputs& in, const float* si
   mla::DecodeParams d = make_params(plan, in);
   d.items = sp.items;
   d.n_items = sp.n_items;
+  d.worker_first = sp.worker_first;
   d.final_mode = 0;
   d.sinks = sinks;
   d.out = out;
   d.lse = lse;
   d.segm_out = reinterpret_cast<float*>(ws + plan->segm_output_offset);
+  d.segm_rows = static_cast<int64_t>(plan->split_items) * plan->tile_rows;
   d.segm_max = reinterpret_cast<float*>(ws + plan->segm_max_offset);
   d.segm_expsum = reinterpret_cast<float*>(ws + plan->segm_expsum_offset);
   return launch_decode(plan, d, reinterpret_cast<int*>(ws + plan->status_offset), stream);
@@ -264,7 +279,7 @@ mla_status_t run_merge_items(const mla_plan_t* plan, const Inputs& in, const flo
   m.lse = lse;
   m.unit_tab = sp.unit_tab;
   m.tiles_max = plan->row_tiles;
-  m.tile_rows = plan->rows_per_cta;
+  m.tile_rows = plan->tile_rows;
   m.sparse = sp.sparse;
   return cuda_status(mla::launch_merge(m, stream));
 }
@@ -287,7 +302,7 @@ const char* mla_status_string(mla_status_t s) {
 
 const char* mla_last_cuda_error(void) { return g_last_cuda_error; }
 
-int32_t mla_version(void) { return 100; }
+int32_t mla_version(void) { return 101; }
 
 mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   if (prob == nullptr || plan == nullptr) return MLA_ERR_INVALID_ARG;
@@ -319,14 +334,14 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   const bool use_rn = p.kernel == MLA_KERNEL_TCGEN05_ROWS_N || (p.kernel == MLA_KERNEL_AUTO && rn_ok);
   const bool use_pair = !use_rn && tc_ok && p.kernel != MLA_KERNEL_WARP_MMA;
   const bool use_tc = use_rn || use_pair;
-  int32_t kernel, rows;
+  int32_t kernel, rows, cluster = 1;
   if (use_rn) {
-    // up to 64 rows per CTA; more rows take several tiles of equal size,
-    // each a CTA of its own over the request's keys (the tiles of a request
-    // run side by side, so that all but the first read the KV from L2)
+    // up to 64 rows on one CTA; 65..128 rows on a cluster of two CTAs of
+    // equal row counts, which share one pass over the request's keys
     kernel = mla::kTcRowsN;
-    const int64_t tiles = (rows_per_unit + 63) / 64;
-    rows = static_cast<int32_t>(((rows_per_unit + tiles - 1) / tiles + 15) / 16 * 16);
+    cluster = rows_per_unit > 64 ? 2 : 1;
+    rows = static_cast<int32_t>(((rows_per_unit + cluster - 1) / cluster + 15) / 16 * 16);
+    if (rows < 16) rows = 16;
   } else if (use_pair) {
     kernel = mla::kTcPair128;
     rows = 128;
@@ -340,7 +355,8 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
     kernel = mla::kMmaRows64;
     rows = 64;
   }
-  const int32_t row_tiles = static_cast<int32_t>((rows_per_unit + rows - 1) / rows);
+  const int32_t tile_rows = rows * cluster;  // rows of a row tile, one per CTA (cluster, pair)
+  const int32_t row_tiles = static_cast<int32_t>((rows_per_unit + tile_rows - 1) / tile_rows);
   const int32_t tile = sparse ? kSparseTile : tile_for_block(p.block_size);
   const int32_t max_len = sparse ? p.topk : p.max_seq_len;
 
@@ -367,21 +383,31 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
   plan->tile_size = tile;
   plan->kernel = kernel;
   plan->rows_per_cta = rows;
+  plan->tile_rows = tile_rows;
   plan->row_tiles = row_tiles;
-  plan->grid_x = use_pair ? 2 * row_tiles : row_tiles;  // a CTA pair per row tile
+  plan->grid_x = use_pair ? 2 * row_tiles : row_tiles * cluster;  // CTAs per row tile
   plan->grid_y = ns;
   plan->grid_z = units;
   plan->status_offset = 0;
   plan->workspace_bytes = kWsAlign;
   if (balanced) {
-    // workers: CTA pairs of the 128-row kernel, CTAs of the rows-as-N kernel
-    const int32_t workers = use_pair ? (sms / 2 > 0 ? sms / 2 : 1) : (sms > 0 ? sms : 1);
+    // workers: CTA pairs of the 128-row kernel; CTAs or clusters of the
+    // rows-as-N kernel, as many as can be resident at once
+    int32_t workers = use_pair || cluster == 2 ? sms / 2 : sms;
+    if (use_rn && cluster == 2 && p.num_sms == 0) {
+      int pairs = 0;
+      const cudaError_t e = mla::decode_hn_max_pairs(rows, &pairs);
+      if (e != cudaSuccess) return cuda_status(e);
+      if (pairs > 0 && pairs < workers) workers = pairs;
+    }
+    if (workers < 1) workers = 1;
+    if (workers > kMaxWorkers) workers = kMaxWorkers;
     const int32_t split_cap = 2 * workers;
     plan->schedule = 1;
     plan->split_items = split_cap;
     plan->max_items = static_cast<int32_t>(unit_tiles + workers);  // rows + cuts
     const SchedLayout l = sched_layout(plan);
-    const size_t slot_rows = static_cast<size_t>(split_cap) * rows;
+    const size_t slot_rows = static_cast<size_t>(split_cap) * tile_rows;
     const size_t out_b = align_up(slot_rows * kRank * sizeof(float), kWsAlign);
     const size_t max_b = align_up(slot_rows * sizeof(float), kWsAlign);
     plan->segm_output_offset = l.end;

@@ -13,7 +13,7 @@ enum KernelId : int32_t {
   kMmaRows32 = 2,   // 32 rows per CTA
   kMmaRows64 = 3,   // 64 rows per CTA
   kTcPair128 = 4,   // tcgen05 CTA-pair kernel, 128 rows per pair
-  kTcRowsN = 5,     // tcgen05 kernel with the query rows as N, 16..64 rows per CTA
+  kTcRowsN = 5,     // tcgen05 kernel with the query rows as N, 16..64 rows per CTA, 1-2 CTAs per tile
 };
 
 struct DecodeParams {
@@ -31,7 +31,8 @@ struct DecodeParams {
   float kv_scale;
   const float* sinks;            // [H] or null (final mode only)
   int32_t final_mode;            // 1: write out/lse; 0: write segment partials
-  float* segm_out;               // [T, H, NS, 512]
+  float* segm_out;               // [T, H, NS, 512]; balanced schedule: [segm_rows, 512] slots
+  int64_t segm_rows;
   float* segm_max;               // [T, H, NS]
   float* segm_expsum;            // [T, H, NS]
   void* out;                     // [T, H, 512] bf16
@@ -41,6 +42,9 @@ struct DecodeParams {
   // at items[8 i ..]; null selects the uniform NS partition
   const int32_t* items;
   const int32_t* n_items;
+  // rows-as-N kernel: worker w (CTA or cluster) runs items
+  // [worker_first[w], worker_first[w + 1]) in order
+  const int32_t* worker_first;
   // bounded waits of the tensor-core kernels give up after this many
   // nanoseconds (0: the default, 2 s)
   uint64_t wait_ns;
@@ -57,6 +61,11 @@ struct SchedParams {
   int32_t* items;                // [max_items, 8]
   int32_t* n_items;              // [1]
   int32_t* unit_tab;             // [num_units * tiles_max, 2]: first partial slot (-1), pieces
+  // contiguous mode (non-null): items in sequence order, cut at every
+  // multiple of cdiv(total, workers) groups, worker w's first item at
+  // worker_first[w] ([workers + 1]); else longest first for one-item CTAs
+  int32_t* worker_first;
+  int32_t workers;
 };
 
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);
@@ -135,9 +144,15 @@ cudaError_t launch_decode_tc(const DecodeParams& p, bool fp8, int64_t q_rows, in
                              dim3 grid, int* status, cudaStream_t stream);
 
 // tcgen05 kernel with the query rows as the MMA N dimension (e4m3, dense,
-// block size a multiple of 64): rows = 16, 32, 48 or 64 query rows per CTA.
-cudaError_t launch_decode_hn(const DecodeParams& p, int rows, int64_t q_rows, int64_t kv_rows,
+// block size a multiple of 64): rows = 16, 32, 48 or 64 query rows per CTA,
+// `cluster` (1, or 2 with 48 or 64 rows) CTAs per row tile sharing its key
+// boxes. With the balanced schedule the grid holds one CTA (cluster) per
+// worker.
+cudaError_t launch_decode_hn(const DecodeParams& p, int rows, int cluster, int64_t q_rows, int64_t kv_rows,
                              dim3 grid, int* status, cudaStream_t stream);
+// Clusters of two CTAs of `rows` rows that can be resident at once on the
+// current device.
+cudaError_t decode_hn_max_pairs(int rows, int* n);
 
 // Shared memory bytes a decode variant needs (host query for validation).
 int decode_mma_smem_bytes(int32_t kernel, bool fp8);

@@ -22,6 +22,13 @@
 // count, from which the merge finds them. Cuts number
 // fewer than the workers, so the slots of split rows number at most two per
 // worker and the items at most rows + workers.
+//
+// Contiguous mode (the rows-as-N kernel, whose workers run many items each):
+// every multiple of W inside a row is a cut, so that worker w's share is
+// exactly the groups [w W, (w + 1) W) of the sequence, and the items are
+// written in sequence order with worker_first[w] = the first item of worker
+// w (a piece belongs to the worker its first group falls to; an empty row,
+// to the worker of its position).
 #include "common.cuh"
 #include "internal.h"
 
@@ -90,7 +97,8 @@ __device__ I block_exclusive_scan(I v, long long* red, I* total) {
 }
 
 // Cuts of the row occupying groups [a, a + g) of the sequence: multiples of
-// W strictly inside, none within W / 8 of either end. Returns their number
+// W strictly inside, none within W / 8 of either end (unless `every`: all of
+// them). Returns their number
 // and the first one. I is int when the whole sequence fits (the usual case:
 // 32-bit division is far cheaper), else long long.
 template <typename I>
@@ -100,8 +108,8 @@ struct Cuts {
 };
 
 template <typename I>
-__device__ __forceinline__ Cuts<I> row_cuts(I a, int g, I W) {
-  const I d = W / 8;
+__device__ __forceinline__ Cuts<I> row_cuts(I a, int g, I W, bool every = false) {
+  const I d = every ? 0 : W / 8;
   const I lo = a + d + 1, hi = a + g - d - 1;  // allowed cut positions
   Cuts<I> c{0, 0};
   if (g > 0 && hi >= lo) {
@@ -206,6 +214,72 @@ __device__ void schedule_items(const SchedParams& p, Info info, I W, long long* 
   if (tid == 0) *p.n_items = static_cast<int32_t>(n_items);
 }
 
+// Contiguous mode: items in sequence order and each worker's first item.
+template <typename I, typename Info>
+__device__ void schedule_contiguous(const SchedParams& p, Info info, I W, int workers, long long* red,
+                                    int* owned) {
+  const int tid = threadIdx.x;
+  const int U = p.num_units;
+  for (int w = tid; w < workers; w += kThreads) owned[w] = 0;
+  __syncthreads();
+  I carry = 0;
+  int piece_carry = 0, slot_carry = 0;
+  for (int u0 = 0; u0 < U; u0 += kThreads) {
+    const int u = u0 + tid;
+    UnitInfo i{0, 0};
+    if (u < U) i = info(u);
+    I sum;
+    const I pos = carry + block_exclusive_scan<I>(static_cast<I>(i.tiles) * i.groups, red, &sum);
+    carry += sum;
+    int npieces = 0, nslots = 0;
+    for (int t = 0; t < i.tiles; ++t) {
+      const Cuts<I> c = row_cuts<I>(pos + static_cast<I>(t) * i.groups, i.groups, W, true);
+      npieces += c.count + 1;
+      if (c.count > 0) nslots += c.count + 1;
+    }
+    int piece_sum, slot_sum;
+    int at = piece_carry + block_exclusive_scan<int>(npieces, red, &piece_sum);
+    piece_carry += piece_sum;
+    int slot = slot_carry + block_exclusive_scan<int>(nslots, red, &slot_sum);
+    slot_carry += slot_sum;
+    for (int t = 0; t < i.tiles; ++t) {
+      const I a = pos + static_cast<I>(t) * i.groups;
+      const Cuts<I> c = row_cuts<I>(a, i.groups, W, true);
+      const int k = c.count + 1;
+      const int pbase = k > 1 ? slot : -1;
+      reinterpret_cast<int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + t] = make_int2(pbase, k);
+      I prev = a;
+      for (int j = 0; j < k; ++j, ++at) {
+        const I next = j < c.count ? c.first + j * W : a + i.groups;
+        const long long owner = min(static_cast<long long>(prev / W), static_cast<long long>(workers - 1));
+        atomicAdd(&owned[owner], 1);
+        int4* it = reinterpret_cast<int4*>(p.items) + 2 * static_cast<int64_t>(at);
+        const long long kb = static_cast<long long>(prev - a) * kGroupKeys;
+        const long long ke = static_cast<long long>(next - a) * kGroupKeys;
+        it[0] = make_int4(u, t, static_cast<int>(min(kb, static_cast<long long>(INT32_MAX))),
+                          static_cast<int>(min(ke, static_cast<long long>(INT32_MAX))));
+        it[1] = make_int4(k > 1 ? pbase + j : -1, 0, 0, 0);
+        prev = next;
+      }
+      if (k > 1) slot += k;
+    }
+  }
+  __syncthreads();
+  // worker_first: exclusive scan of the pieces each worker owns
+  int first = 0;
+  for (int w0 = 0; w0 < workers; w0 += kThreads) {
+    const int w = w0 + tid;
+    int all;
+    const int ex = block_exclusive_scan<int>(w < workers ? owned[w] : 0, red, &all);
+    if (w < workers) p.worker_first[w] = first + ex;
+    first += all;
+  }
+  if (tid == 0) {
+    p.worker_first[workers] = first;
+    *p.n_items = first;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams p) {
   // the decode kernel may launch now; it waits for this grid before reading
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -233,6 +307,15 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams
     total += static_cast<long long>(i.tiles) * i.groups;
   }
   total = block_sum(total, red);  // (its barriers also publish the cache)
+  if (p.worker_first != nullptr) {
+    const int workers = p.workers > 0 ? (p.workers < kSizeBins ? p.workers : kSizeBins) : 1;
+    const long long W = total > 0 ? (total + workers - 1) / workers : 1;
+    if (total < (1ll << 30))
+      schedule_contiguous<int>(p, info, static_cast<int>(W), workers, red, hist);
+    else
+      schedule_contiguous<long long>(p, info, W, workers, red, hist);
+    return;
+  }
   const long long workers = p.split_cap / 2 > 0 ? p.split_cap / 2 : 1;
   const long long W = total > 0 ? (total + workers - 1) / workers : 1;
   if (total < (1ll << 30))

@@ -24,6 +24,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
 }
+// arrive.expect_tx on an mbarrier of another CTA of the cluster (address
+// from mapa): that CTA's phase then also waits for `bytes` more bytes.
+__device__ __forceinline__ void mbar_arrive_expect_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;\n" ::"r"(cluster_bar),
+               "r"(bytes)
+               : "memory");
+}
 // Arrive on an mbarrier of another CTA of the cluster (address from mapa).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_bar)
@@ -127,6 +134,11 @@ template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;\n" ::"n"(N) : "memory");
 }
+__device__ __forceinline__ int ld_cluster_s32(uint32_t caddr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];\n" : "=r"(v) : "r"(caddr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(caddr), "f"(v) : "memory");
 }
@@ -160,6 +172,24 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const void* tmap,
       " [%0], [%1, {%2, %3}], [%4], %5;\n" ::"r"(dst),
       "l"(tmap), "r"(x), "r"(y), "r"(bar), "l"(pol)
       : "memory");
+}
+// tma_load_2d_hint delivering the box to the same shared-memory offset in
+// every CTA of the cluster whose bit is set in cta_mask, each completing the
+// transaction on its own barrier at the offset of `bar`.
+__device__ __forceinline__ void tma_load_2d_mc_hint(uint32_t dst, const void* tmap, int x, int y, uint32_t bar,
+                                                    uint16_t cta_mask, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;\n" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(bar), "h"(cta_mask), "l"(pol)
+      : "memory");
+}
+// Store of a box from this CTA's shared memory to a 3-D tensor at (x, y, z),
+// tracked by the thread's bulk async-groups (commit with bulk_commit_group).
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];\n" ::"l"(tmap),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
 }
 // Four rows r0..r3 of a 2-D tensor whose map has a one-row box, each the
 // box's width from column x, to consecutive rows of the destination

@@ -1,6 +1,7 @@
 // tma_map.cuh -- host-side TMA tensor maps over [rows, 576] row tensors (q
 // and the KV cache viewed as rows), 128-byte-wide boxes with the 128-byte
-// swizzle the tcgen05 shared-memory descriptors of the decode kernels expect.
+// swizzle the tcgen05 shared-memory descriptors of the decode kernels expect;
+// and over the [rows, mid, 512] outputs the decode stores.
 #pragma once
 
 #include <atomic>
@@ -42,6 +43,24 @@ inline cudaError_t make_row_map(CUtensorMap* m, const void* base, uint64_t rows,
   CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// 3-D map over an output tensor [rows, mid, 512] of fp32 (or bf16 with
+// `bf16`) values, row stride mid * 512 elements, for stores of 8-row x
+// 32-column boxes (one box column at a time along `mid`), no swizzle.
+inline cudaError_t make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t mid, bool bf16) {
+  auto enc = tma_encode_fn();
+  if (enc == nullptr) return cudaErrorNotSupported;
+  const uint64_t elt = bf16 ? 2 : 4;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(512), static_cast<cuuint64_t>(mid), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(512 * elt), static_cast<cuuint64_t>(512 * elt * mid)};
+  cuuint32_t box[3] = {32, 1, 8};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

@@ -43,8 +43,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_struct_sizes_match_the_header(lib):
     assert ctypes.sizeof(B.Problem) == 17 * 4
-    # 17 problem ints + 9 plan ints + 4 reserved + 5 size_t
-    assert ctypes.sizeof(B.Plan) == 160
+    # 17 problem ints + 14 plan ints (+ 4 bytes of padding) + 5 size_t; the
+    # library asserts the same size at compile time
+    assert ctypes.sizeof(B.Plan) == 168
 
 
 def test_status_strings(lib):
@@ -266,10 +267,11 @@ def test_plan_balanced_schedule(lib):
 def test_plan_rows_as_n(lib, heads, qlen, rows):
     """e4m3 requests of at most 64 query rows go to the rows-as-N kernel (one
     CTA per row tile, one worker per SM under the balanced schedule, partial
-    slots of rows_per_cta rows); wider ones stay on the CTA pair."""
+    slots of tile_rows rows); wider ones stay on the CTA pair."""
     prob = _dense_problem(dtype="fp8", num_heads=heads, num_tokens=64 * qlen, max_qlen=qlen)
     plan = B.mla_decode_plan(prob)
     assert plan.kernel == 5 and plan.rows_per_cta == rows and plan.row_tiles == 1
+    assert plan.tile_rows == rows and plan.grid_x == 1
     assert plan.schedule == 1 and plan.split_items == 2 * 152 and plan.max_items == 64 + 152
     slot_rows = plan.split_items * rows
     assert plan.segm_max_offset - plan.segm_output_offset >= slot_rows * 512 * 4
@@ -278,11 +280,29 @@ def test_plan_rows_as_n(lib, heads, qlen, rows):
     # the CTA pair and the warp-MMA kernel can still be asked for
     assert B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=heads, num_tokens=64 * qlen,
                                             max_qlen=qlen, kernel=B.MLA_KERNEL_TCGEN05)).kernel == 4
-    # 65-128 rows: two row tiles of equal size; more rows go to the CTA pair
-    two = B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=96))
-    assert two.kernel == 5 and two.row_tiles == 2 and two.rows_per_cta == 48
+    # more rows go to the CTA pair
     wide = B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=128, num_tokens=128, max_qlen=2))
     assert wide.kernel == 4
+
+
+@pytest.mark.parametrize("heads,qlen,rows", [(96, 1, 48), (128, 1, 64), (65, 1, 48), (40, 3, 64),
+                                             (33, 2, 48)])
+def test_plan_rows_as_n_cluster(lib, heads, qlen, rows):
+    """65..128 query rows: one row tile on a cluster of two CTAs of equal row
+    counts (one pass over the keys for all heads), a worker per two SMs, and
+    partial slots of the whole tile."""
+    prob = _dense_problem(dtype="fp8", num_heads=heads, num_tokens=64 * qlen, max_qlen=qlen)
+    plan = B.mla_decode_plan(prob)
+    assert plan.kernel == 5 and plan.rows_per_cta == rows and plan.tile_rows == 2 * rows
+    assert plan.row_tiles == 1 and plan.grid_x == 2
+    assert plan.schedule == 1 and plan.split_items == 2 * 76 and plan.max_items == 64 + 76
+    slot_rows = plan.split_items * 2 * rows
+    assert plan.segm_max_offset - plan.segm_output_offset >= slot_rows * 512 * 4
+    assert plan.workspace_bytes >= plan.segm_expsum_offset + slot_rows * 4
+    uniform = B.mla_decode_plan(_dense_problem(dtype="fp8", num_heads=heads, num_tokens=64 * qlen,
+                                               max_qlen=qlen, num_segments=3))
+    assert uniform.schedule == 0 and uniform.kernel == 5 and uniform.grid_x == 2
+    assert uniform.grid_y == 3 and uniform.tile_rows == 2 * rows
 
 
 def test_schedule_stages_reject_bad_arguments(lib):
@@ -372,15 +392,19 @@ def test_plan_random_problems_are_consistent(lib):
                  and heads * prob.max_qlen <= 128)
         if rn_ok:  # the planner's first choice wherever it can run
             rows = heads * prob.max_qlen
-            tiles = -(-rows // 64)
-            assert plan.kernel == 5 and plan.row_tiles == tiles and plan.grid_x == tiles
-            assert plan.rows_per_cta == -(-(-(-rows // tiles)) // 16) * 16
+            cl = 2 if rows > 64 else 1
+            assert plan.kernel == 5 and plan.row_tiles == 1 and plan.grid_x == cl
+            assert plan.rows_per_cta == max(16, -(-(-(-rows // cl)) // 16) * 16)
+            assert plan.tile_rows == cl * plan.rows_per_cta
+        elif plan.kernel == 4:
+            assert plan.tile_rows == plan.rows_per_cta == 128
         if plan.schedule == 1:
             assert plan.kernel in (4, 5) and ns == 0 and plan.num_segments == 1
-            workers = max(1, sms // 2) if plan.kernel == 4 else sms
+            pairs = plan.kernel == 4 or plan.tile_rows > plan.rows_per_cta
+            workers = min(1024, max(1, sms // 2) if pairs else sms)
             assert plan.split_items == 2 * workers
             assert plan.max_items == units * plan.row_tiles + workers
-            rows = plan.split_items * plan.rows_per_cta
+            rows = plan.split_items * plan.tile_rows
             assert plan.segm_output_offset >= 512 + plan.max_items * 32
             assert plan.segm_max_offset >= plan.segm_output_offset + rows * 512 * 4
             assert plan.segm_expsum_offset >= plan.segm_max_offset + rows * 4

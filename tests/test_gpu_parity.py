@@ -507,7 +507,7 @@ def test_full_dsv3_bf16_sampled(kernel):
 @pytest.mark.parametrize("heads", [96, 128])
 def test_fp8_planner_path_split_rows(heads, kernel):
     # e4m3 above 64 heads under the balanced schedule: the planner's default
-    # (the rows-as-N kernel, two row tiles per request) and the CTA pair;
+    # (the rows-as-N kernel, a cluster of two CTAs per request) and the CTA pair;
     # 6 requests x 4096 keys on 76-152 workers split every row
     w = I.fp8_decode(heads, batch=6, seq_len=4096, num_segments=0)
     out, lse, dw = run_gpu(w, kernel=kernel)

@@ -61,3 +61,56 @@ def test_cut_rule_stays_inside_the_workspace(name, pairs):
         if len(p) > 1:                             # no sliver next to a row's ends
             assert p[0] > W // 8 and p[-1] > W // 8
             assert all(x <= W for x in p[1:-1])
+
+
+def contiguous_rule(groups, tiles, workers):
+    """The rows-as-N kernel's schedule: every multiple of W inside a row is a
+    cut, items in sequence order, a piece owned by the worker its first group
+    falls to (an empty row: the worker of its position, at most the last).
+    Returns the items [(unit, tile, first group, end group, partial slot or
+    -1)], worker_first and W."""
+    total = sum(g * t for g, t in zip(groups, tiles))
+    W = -(-total // workers) if total > 0 else 1
+    items, owners, pos, slot = [], [], 0, 0
+    for u, (g, t) in enumerate(zip(groups, tiles)):
+        for tt in range(t):
+            a, b = pos, pos + g
+            cuts = list(range((a // W + 1) * W, b, W)) if g > 1 else []
+            bounds = [a] + cuts + [b]
+            k = len(bounds) - 1
+            for j in range(k):
+                items.append((u, tt, bounds[j] - a, bounds[j + 1] - a, slot + j if k > 1 else -1))
+                owners.append(min(bounds[j] // W, workers - 1))
+            if k > 1:
+                slot += k
+            pos = b
+    first = [int(np.searchsorted(owners, w, side="left")) for w in range(workers)] + [len(items)]
+    return items, first, W
+
+
+@pytest.mark.parametrize("workers", [1, 7, 76, 152])
+@pytest.mark.parametrize("name", sorted(CASES) + ["random"])
+def test_contiguous_rule_balances_exactly(name, workers):
+    if name == "random":
+        rng = np.random.default_rng(workers + 1000)
+        groups = rng.integers(0, 600, size=300).tolist()
+        tiles = rng.integers(1, 3, size=300).tolist()
+    else:
+        groups, tiles = CASES[name]
+    items, first, W = contiguous_rule(groups, tiles, workers)
+    rows = sum(tiles)
+    total = sum(g * t for g, t in zip(groups, tiles))
+    assert len(items) <= rows + workers                          # plan: max_items
+    assert len({it[4] for it in items if it[4] >= 0}) == sum(it[4] >= 0 for it in items)
+    assert all(it[4] < 2 * workers for it in items)              # plan: split_items slots
+    assert first[0] == 0 and first[-1] == len(items) and np.all(np.diff(first) >= 0)
+    # worker w's pieces are exactly the groups [w W, (w + 1) W) of the sequence
+    for w in range(workers):
+        load = sum(it[3] - it[2] for it in items[first[w]:first[w + 1]])
+        assert load == max(0, min(W, total - w * W)), (w, load)
+    # each row covered once, in order
+    for u, (g, t) in enumerate(zip(groups, tiles)):
+        for tt in range(t):
+            mine = [it for it in items if it[0] == u and it[1] == tt]
+            assert mine[0][2] == 0 and mine[-1][3] == g
+            assert all(x[3] == y[2] for x, y in zip(mine, mine[1:]))
