@@ -67,11 +67,13 @@ using namespace tc;
 constexpr int kKeys = 128;               // keys per chunk: M of QK^T, K of P.V
 constexpr int kHalf = 64;                // keys per TMA box (rows of one block)
 constexpr int kSlot = kKeys * 128;       // ring slot: one 128-byte column box of a chunk
+constexpr int kRSlot = kKeys * 64;       // rope ring slot: the chunk's 64 rope columns
 constexpr int kBoxes = 5;                // per chunk: 4 latent boxes (512 e4m3) + the rope box
 constexpr int kThreads = 384;
 constexpr int kProducers = 2;            // warps 0, 2
 constexpr int kSoftWarps = 8;            // warps 4-11: four TMEM lane quarters x two row halves
 constexpr int kMaxSlots = 14;
+constexpr int kMaxRSlots = 4;
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;
 constexpr float kPBias = 4.f;            // p = 2^(s - m_ref + kPBias) <= 2^(2 kPBias)
 constexpr float kMove = 4.f;             // m_ref moves when a chunk max exceeds it by more
@@ -79,15 +81,16 @@ constexpr float kMove = 4.f;             // m_ref moves when a chunk max exceeds
 enum : int {
   kFull = 0,                    // [kMaxSlots] ring slot loaded
   kEmpty = kMaxSlots,           // [kMaxSlots] ring slot released by every CTA of the cluster
-  kQFull = 2 * kMaxSlots,       // q of the current item loaded
+  kRFull = 2 * kMaxSlots,       // [kMaxRSlots] rope slot loaded
+  kREmpty = kRFull + kMaxRSlots,  // [kMaxRSlots] rope slot released by every CTA of the cluster
+  kQFull = kREmpty + kMaxRSlots,  // q of the current item loaded
   kQFree,                       // QK^T of the item complete: q may be replaced
   kSFull,                       // [2] S^T buffer written
   kSFree = kSFull + 2,          // [2] S^T buffer read
   kPFull = kSFree + 2,          // [2] P^T buffer written
   kPFree = kPFull + 2,          // [2] P.V of the buffer's chunk complete
   kXA = kPFree + 2,             // [2] softmax warps: chunk maxima posted
-  kXB = kXA + 2,                // [2] softmax warps: reference maxima moved
-  kXE = kXB + 2,                // epilogue: row sums posted
+  kXE = kXA + 2,                // epilogue: row sums posted
   kXF = kXE + 1,                // epilogue: row factors posted
   kOFull = kXF + 1,             // last P.V of the item complete
   kOFree = kOFull + 1,          // epilogue read O^T: the next item may overwrite it
@@ -100,18 +103,20 @@ enum : int {
 constexpr int kOffBar = 0;
 constexpr int kOffTslot = 512;
 constexpr int kOffAbort = 516;
-constexpr int kOffIssued = 576;             // [kMaxSlots + 1] int: last use issued per ring slot, q
+constexpr int kOffIssued = 576;             // [kMaxSlots + kMaxRSlots + 1] int: last use issued
+                                            // per ring slot, per rope slot, of q
+constexpr int kIssuedQ = kMaxSlots + kMaxRSlots;
 constexpr int kOffWmax = 1024;              // [2][4][64] warp maxima of a chunk
-constexpr int kOffMref = kOffWmax + 2048;   // [64] reference max per row
-constexpr int kOffMtrue = kOffMref + 256;   // [64] true max per row
-constexpr int kOffAlpha = kOffMtrue + 256;  // [2][64] rescale factor per row
-constexpr int kOffResc = kOffAlpha + 512;   // [2] int: some row moved its reference
-constexpr int kOffVis = kOffResc + 256;     // [64] int: causal end of each row
+// per row and chunk parity (written for chunk c, read back at chunk c + 1):
+constexpr int kOffMref = kOffWmax + 2048;   // [2][64] reference max
+constexpr int kOffMtrue = kOffMref + 512;   // [2][64] true max
+constexpr int kOffAlpha = kOffMtrue + 512;  // [2][64] rescale factor
+constexpr int kOffVis = kOffAlpha + 512;    // [64] int: causal end of each row
 constexpr int kOffLsum = kOffVis + 256;     // [4][64] row sums per warp
 constexpr int kOffMult = kOffLsum + 1024;   // [64] output factor per row
 constexpr int kHeader = 6144;
 static_assert(kNumBars * 8 <= kOffTslot, "barrier space");
-static_assert(kOffIssued + 4 * (kMaxSlots + 1) <= 1024, "issue record space");
+static_assert(kOffIssued + 4 * (kIssuedQ + 1) <= 1024, "issue record space");
 static_assert(kOffMult + 256 <= kHeader, "header space");
 
 constexpr int align1k(int v) { return (v + 1023) / 1024 * 1024; }
@@ -131,9 +136,8 @@ struct HnCfg {
   static constexpr int kOffQ = kHeader;
   static constexpr int kPLbo = 16 * NR;             // P^T bytes per 8-key group (hi + lo cores)
   static constexpr int kPBytes = kKeys * 2 * NR;    // one P^T buffer
-  // two P^T buffers (the softmax of chunk c + 1 writes while P.V of chunk c
-  // reads), one at 64 rows, where a second would cost the ring its tenth slot
-  static constexpr int kPBufs = NR == 64 ? 1 : 2;
+  // two P^T buffers: the softmax of chunk c + 1 writes while P.V of chunk c reads
+  static constexpr int kPBufs = 2;
   static constexpr int kOffP = kOffQ + kBoxes * kQBox;
   // the P^T buffers double as the epilogue's output staging (2 KB per
   // softmax warp): P.V of the item is complete and the next item's first
@@ -142,18 +146,26 @@ struct HnCfg {
   static constexpr int kPRegion = kPBufs * kPBytes > kStage ? kPBufs * kPBytes : kStage;
   static constexpr int kOffRing = align1k(kOffP + kPRegion);
   static constexpr int kUsable = 232448 - 1024;     // dynamic shared memory minus alignment slack
-  static constexpr int kSlotsFit = (kUsable - kOffRing) / kSlot;
+  // the rope columns (64 bytes of each key) have a ring of their own, of
+  // 64-byte-wide boxes (in a 128-byte slot they would take twice the
+  // space): the latent ring takes what leaves two rope slots, the rope ring
+  // the rest
+  static constexpr int kSlotsFit = (kUsable - kOffRing - 2 * kRSlot) / kSlot;
   static constexpr int kSlots = kSlotsFit < kMaxSlots ? kSlotsFit : kMaxSlots;
-  static constexpr int kSmem = kOffRing + kSlots * kSlot + 1024;
+  static constexpr int kRSlotsFit = (kUsable - kOffRing - kSlots * kSlot) / kRSlot;
+  static constexpr int kRSlots = kRSlotsFit < kMaxRSlots ? kRSlotsFit : kMaxRSlots;
+  static constexpr int kOffRope = kOffRing + kSlots * kSlot;
+  static constexpr int kSmem = kOffRope + kRSlots * kRSlot + 1024;
   // QK^T of chunk c + 1 is issued before P.V of chunk c, which holds the
   // ring indices of chunk c's value boxes: both chunks must fit the ring
-  static_assert(kSlots >= 2 * kBoxes, "ring slots");
+  static_assert(kSlots >= 2 * (kBoxes - 1) && kRSlots >= 2, "ring slots");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 struct HnMaps {
   CUtensorMap q;     // q viewed as [T*H rows, 576] e4m3, box 128 bytes x NR rows
   CUtensorMap kv;    // cache viewed as [NB*BS rows, 576] e4m3, box 128 bytes x 64 rows
+  CUtensorMap kvr;   // the same, box 64 bytes x 64 rows (the rope columns)
   CUtensorMap out;   // out as [T*H, 1, 512] bf16, box 8 rows x 32 columns
   CUtensorMap part;  // segment partials as [slot rows, 1, 512] or [T*H, NS, 512] fp32
 };
@@ -302,12 +314,12 @@ __device__ __forceinline__ int cache_row(const DecodeParams& p, const int32_t* b
 }
 
 // ------------------------------------------------------------------ producers
-// Box j of the worker's g-th chunk (two 64-row TMA boxes from their blocks)
-// goes to ring slot i % kSlots, i = g * 5 + j, the count running on across
-// the worker's items. Box i is loaded by CTA i % CL of the cluster (the only
-// one in a cluster of one) and there by producer warp (i / CL) % 2, which
-// records the latest use issued per slot (the teardown waits for those
-// loads). The whole warp looks up the cache rows of 16 chunks at a time
+// Latent box j < 4 of the worker's g-th chunk (two 64-row TMA boxes from
+// their blocks) goes to ring slot i % kSlots, i = 4 g + j, its rope box to
+// rope slot g % kRSlots, the counts running on across the worker's items.
+// Box b = 5 g + j is loaded by CTA b % CL of the cluster (the only one in a
+// cluster of one) and there by producer warp (b / CL) % 2, which records
+// the latest use issued per slot (the teardown waits for those loads). The whole warp looks up the cache rows of 16 chunks at a time
 // (lane l: chunk l / 2, half l % 2), one window ahead of the chunks it
 // issues, so that no TMA issue waits on a block-table read; lane 0 issues.
 template <int NR, int CL>
@@ -315,7 +327,10 @@ __device__ void produce(const Ctx& x, const HnMaps& maps, const DecodeParams& p,
   using C = HnCfg<NR>;
   const int lane = x.lane;
   volatile int* issued = reinterpret_cast<volatile int*>(x.smem + kOffIssued);
-  if (lane == 0) tma_prefetch_desc(&maps.kv);
+  if (lane == 0) {
+    tma_prefetch_desc(&maps.kv);
+    tma_prefetch_desc(&maps.kvr);
+  }
   const uint64_t pol = l2_evict_first();  // each key row is read once
   int gb = 0;                             // the worker's box count
   bool ok = true;
@@ -339,30 +354,36 @@ __device__ void produce(const Ctx& x, const HnMaps& maps, const DecodeParams& p,
       const bool two = it.seg_start + c * kKeys + kHalf < it.seg_end;
       if (lane == 0) {
         for (int j = 0; j < kBoxes; ++j) {
-          const int ii = gb + j;
-          if (ii % CL != x.rank || (ii / CL) % kProducers != pidx) continue;
-          const int slot = ii % C::kSlots;
-          const int use = ii / C::kSlots;
-          if (use >= 1 && !wait_phase<(CL > 1)>(x, x.bar(kEmpty + slot), (use - 1) & 1, 11)) {
+          const int bi = gb + j;
+          if (bi % CL != x.rank || (bi / CL) % kProducers != pidx) continue;
+          const bool rope = j == kBoxes - 1;
+          const int i = rope ? gb / kBoxes : (gb / kBoxes) * (kBoxes - 1) + j;
+          const int nslots = rope ? C::kRSlots : C::kSlots;
+          const int slot = i % nslots;
+          const int use = i / nslots;
+          const int empty = rope ? kREmpty + slot : kEmpty + slot;
+          if (use >= 1 && !wait_phase<(CL > 1)>(x, x.bar(empty), (use - 1) & 1, 11)) {
             ok = false;
             break;
           }
-          const uint32_t bytes = two ? kSlot : kSlot / 2;
-          const uint32_t full = x.bar(kFull + slot);
+          const int box = rope ? kRSlot : kSlot;
+          const uint32_t bytes = two ? box : box / 2;
+          const uint32_t full = x.bar(rope ? kRFull + slot : kFull + slot);
           mbar_arrive_expect_tx(full, bytes);
-          const uint32_t dst = smem_u32(x.smem + C::kOffRing + slot * kSlot);
+          const uint32_t dst = smem_u32(x.smem + (rope ? C::kOffRope + slot * kRSlot : C::kOffRing + slot * kSlot));
+          const CUtensorMap* map = rope ? &maps.kvr : &maps.kv;
           if constexpr (CL == 1) {
-            tma_load_2d_hint(dst, &maps.kv, 128 * j, row0, full, pol);
-            if (two) tma_load_2d_hint(dst + kSlot / 2, &maps.kv, 128 * j, row1, full, pol);
+            tma_load_2d_hint(dst, map, 128 * j, row0, full, pol);
+            if (two) tma_load_2d_hint(dst + box / 2, map, 128 * j, row1, full, pol);
           } else {
             // the peers' phases of this slot also wait for the box
             for (int r = 0; r < CL; ++r)
               if (r != x.rank) mbar_arrive_expect_tx_cluster(map_to_rank(full, r), bytes);
             constexpr uint16_t kAll = static_cast<uint16_t>((1u << CL) - 1u);
-            tma_load_2d_mc_hint(dst, &maps.kv, 128 * j, row0, full, kAll, pol);
-            if (two) tma_load_2d_mc_hint(dst + kSlot / 2, &maps.kv, 128 * j, row1, full, kAll, pol);
+            tma_load_2d_mc_hint(dst, map, 128 * j, row0, full, kAll, pol);
+            if (two) tma_load_2d_mc_hint(dst + box / 2, map, 128 * j, row1, full, kAll, pol);
           }
-          atomicMax(const_cast<int*>(issued + slot), use);
+          atomicMax(const_cast<int*>(issued + (rope ? kMaxSlots + slot : slot)), use);
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -387,6 +408,7 @@ __device__ void qk_issue(const Ctx& x, const HnMaps& maps, const DecodeParams& p
   constexpr uint32_t kIdQK = instr_desc(128, NR, 0, 0, false, false);
   const uint64_t q_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffQ), 16, 1024);
   const uint64_t k_desc = smem_desc_sw128(smem_u32(x.smem + C::kOffRing), 16, 1024);  // K-major
+  const uint64_t r_desc = smem_desc_sw64(smem_u32(x.smem + C::kOffRope), 512);         // K-major
   volatile int* issued = reinterpret_cast<volatile int*>(x.smem + kOffIssued);
   tma_prefetch_desc(&maps.q);
   int g = 0;   // the worker's chunk count
@@ -401,7 +423,7 @@ __device__ void qk_issue(const Ctx& x, const HnMaps& maps, const DecodeParams& p
     const int qrow = it.tok0 * p.num_heads + it.row0;
     for (int j = 0; j < kBoxes; ++j)
       tma_load_2d(smem_u32(x.smem + C::kOffQ + j * C::kQBox), &maps.q, 128 * j, qrow, x.bar(kQFull));
-    issued[kMaxSlots] = ne;
+    issued[kIssuedQ] = ne;
     if (!wait_phase(x, x.bar(kQFull), ne & 1, 21)) break;
     for (int c = 0; c < it.n_chunks && ok; ++c, ++g) {
       const int b = g & 1;
@@ -412,20 +434,23 @@ __device__ void qk_issue(const Ctx& x, const HnMaps& maps, const DecodeParams& p
       const uint32_t d = x.tbase + C::kSCol + b * NR;
 #pragma unroll
       for (int j = 0; j < kBoxes; ++j) {
-        const int i = g * kBoxes + j;
-        const int slot = i % C::kSlots;
-        if (!wait_phase<(CL > 1)>(x, x.bar(kFull + slot), (i / C::kSlots) & 1, 23)) {
+        const bool rope = j == kBoxes - 1;
+        const int i = rope ? g : g * (kBoxes - 1) + j;
+        const int slot = i % (rope ? C::kRSlots : C::kSlots);
+        const int use = i / (rope ? C::kRSlots : C::kSlots);
+        if (!wait_phase<(CL > 1)>(x, x.bar(rope ? kRFull + slot : kFull + slot), use & 1, 23)) {
           ok = false;
           break;
         }
         fence_after_sync();
-        const uint64_t a = k_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
+        const uint64_t a = rope ? r_desc + static_cast<uint64_t>(slot * (kRSlot >> 4))
+                                : k_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
         const uint64_t qb = q_desc + static_cast<uint64_t>(j * (C::kQBox >> 4));
         // 32 e4m3 columns per instruction: 4 per latent box, 2 for the 64 rope columns
 #pragma unroll
-        for (int s = 0; s < (j < 4 ? 4 : 2); ++s)
+        for (int s = 0; s < (rope ? 2 : 4); ++s)
           mma_ss_f8(d, a + 2 * s, qb + 2 * s, kIdQK, (j | s) != 0 ? 1u : 0u);
-        if (j == 4) release<CL>(x.bar(kEmpty + slot));  // the rope box's only read
+        if (rope) release<CL>(x.bar(kREmpty + slot));  // the rope box's only read
       }
       if (!ok) break;
       mma_commit(x.bar(kSFull + b));
@@ -467,7 +492,7 @@ __device__ void pv_issue(const Ctx& x, const DecodeParams& p) {
       const uint64_t pb = p_desc + static_cast<uint64_t>((g % C::kPBufs) * (C::kPBytes >> 4));
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
-        const int slot = (g * kBoxes + m) % C::kSlots;
+        const int slot = (g * (kBoxes - 1) + m) % C::kSlots;
         const uint64_t a = v_desc + static_cast<uint64_t>(slot * (kSlot >> 4));
         const uint32_t dm = x.tbase + m * C::kNpv;
 #pragma unroll
@@ -538,7 +563,6 @@ __device__ void softmax_rows(const Ctx& x, const HnMaps& maps, const DecodeParam
   float* mref = reinterpret_cast<float*>(x.smem + kOffMref);
   float* mtrue = reinterpret_cast<float*>(x.smem + kOffMtrue);
   float* alpha = reinterpret_cast<float*>(x.smem + kOffAlpha);
-  int* resc = reinterpret_cast<int*>(x.smem + kOffResc);
   int* vis = reinterpret_cast<int*>(x.smem + kOffVis);
   float* lsum = reinterpret_cast<float*>(x.smem + kOffLsum);
   float* mult = reinterpret_cast<float*>(x.smem + kOffMult);
@@ -585,30 +609,39 @@ __device__ void softmax_rows(const Ctx& x, const HnMaps& maps, const DecodeParam
         const float r = warp_max_f32(s[n]);
         if (lane == (n & 31)) wmax[(b * 4 + q4) * 64 + r0 + n] = r;
       }
-      if (t8 == 0) resc[b] = 0;
       ok = cross_sync(x, kXA + b, par, 32);
       if (!ok) break;
-      if (t8 < NR) {
-        const float* w = wmax + b * 256 + t8;
+      // each warp moves the reference of its own rows (lane l: row r0 + l),
+      // from the previous chunk's copy to this chunk's: the four warps of a
+      // row half compute, and write, the same values
+      float* mr = mref + b * 64;
+      float* mt = mtrue + b * 64;
+      float* al = alpha + b * 64;
+      bool moved = false;
+      if (lane < NH) {
+        const int r = r0 + lane;
+        const float* w = wmax + b * 256 + r;
         const float mc = fmaxf(fmaxf(w[0], w[64]), fmaxf(w[128], w[192])) * scale2;
-        mtrue[t8] = fmaxf(mtrue[t8], mc);
-        const float mo = mref[t8];
-        float a = 1.f;
+        const float mo = mref[(b ^ 1) * 64 + r];
+        mt[r] = fmaxf(mtrue[(b ^ 1) * 64 + r], mc);
+        float a = 1.f, m = mo;
         if (mc > mo + kMove) {  // also when the row's first visible key arrives
           if (mo != -INFINITY) {
             a = fast_exp2(mo - mc);
-            resc[b] = 1;
+            moved = true;
           }
-          mref[t8] = mc;
+          m = mc;
         }
-        alpha[b * 64 + t8] = a;
+        mr[r] = m;
+        al[r] = a;
       }
-      ok = cross_sync(x, kXB + b, par, 33);
-      if (!ok) break;
-      if (resc[b] != 0) {
-        // some rows' reference moved: their sums and O^T columns are rescaled
+      moved = __any_sync(0xffffffffu, moved);
+      __syncwarp();
+      if (moved) {
+        // some of this warp's rows moved their reference: their sums and its
+        // part of their O^T columns are rescaled
 #pragma unroll
-        for (int n = 0; n < NH; ++n) l[n] *= alpha[b * 64 + r0 + n];
+        for (int n = 0; n < NH; ++n) l[n] *= al[r0 + n];
         if (c > 0) {  // O^T holds P.V of the item's chunks < c: wait for the last of them
           ok = warp_wait(x, x.bar(kPFree + ((g - 1) & 1)), ((g - 1) >> 1) & 1, 34);
           if (!ok) break;
@@ -625,7 +658,7 @@ __device__ void softmax_rows(const Ctx& x, const HnMaps& maps, const DecodeParam
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 8; ++i)
-                  r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha[b * 64 + r0 + 8 * u + i]);
+                  r[i] = __float_as_uint(__uint_as_float(r[i]) * al[r0 + 8 * u + i]);
                 tmem_st_32x32b_x8(ta + 8 * u, r);
               }
             }
@@ -653,7 +686,7 @@ __device__ void softmax_rows(const Ctx& x, const HnMaps& maps, const DecodeParam
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int n = 8 * u + 4 * q + 2 * e;  // row index within the warp's rows
-            const float2 m2 = *reinterpret_cast<const float2*>(mref + r0 + n);
+            const float2 m2 = *reinterpret_cast<const float2*>(mr + r0 + n);
             const float b0 = m2.x == -INFINITY ? 0.f : m2.x - kPBias;
             const float b1 = m2.y == -INFINITY ? 0.f : m2.y - kPBias;
             const float p0 = fast_exp2(fmaf(s[n], scale2, -b0));
@@ -679,7 +712,7 @@ __device__ void softmax_rows(const Ctx& x, const HnMaps& maps, const DecodeParam
         for (int mm = 0; mm < 2; ++mm) {
           const int m = 2 * (sw >> 2) + mm;
           uint4* row = reinterpret_cast<uint4*>(x.smem + C::kOffRing +
-                                                ((g * kBoxes + m) % C::kSlots) * kSlot + k * 128);
+                                                ((g * (kBoxes - 1) + m) % C::kSlots) * kSlot + k * 128);
 #pragma unroll
           for (int q = 0; q < 8; ++q) row[q] = z;
         }
@@ -707,10 +740,13 @@ __device__ void softmax_rows(const Ctx& x, const HnMaps& maps, const DecodeParam
     ok = cross_sync(x, kXE, ni & 1, 37);
     if (!ok) break;
     if (t8 < 64) {
+      // the item's last chunk left the row state in buffer (g - 1) & 1,
+      // which the next item's first chunk reads as its previous state
+      const int lb = ((g - 1) & 1) * 64;
       if (t8 < NR) {
         const int rho = it.row0 + t8;
         const float L = (lsum[t8] + lsum[64 + t8]) + (lsum[128 + t8] + lsum[192 + t8]);
-        const float base = mref[t8] == -INFINITY ? 0.f : mref[t8] - kPBias;  // the sums' reference
+        const float base = mref[lb + t8] == -INFINITY ? 0.f : mref[lb + t8] - kPBias;  // the sums' reference
         float f = 0.f;
         if (rho < it.rows_total) {
           const int tok = it.tok0 + rho / H;
@@ -733,7 +769,7 @@ __device__ void softmax_rows(const Ctx& x, const HnMaps& maps, const DecodeParam
           } else {
             const int64_t ts = it.pslot >= 0 ? static_cast<int64_t>(it.pslot) * (CL * NR) + x.rank * NR + t8
                                              : th * p.num_segments + it.seg;
-            const float mt = mtrue[t8];
+            const float mt = mtrue[lb + t8];
             p.segm_max[ts] = L > 0.f ? mt : -INFINITY;
             p.segm_expsum[ts] = L > 0.f ? L * exp2f(base - mt) : 0.f;
             f = L > 0.f ? 1.f / L : 0.f;
@@ -743,8 +779,8 @@ __device__ void softmax_rows(const Ctx& x, const HnMaps& maps, const DecodeParam
       }
       // row t8's state for the next item (every warp's reads of this item's
       // state are behind the exchange above)
-      mref[t8] = -INFINITY;
-      mtrue[t8] = -INFINITY;
+      mref[lb + t8] = -INFINITY;
+      mtrue[lb + t8] = -INFINITY;
       if (idx + 1 < x.it_end) vis[t8] = visible_end(item_at<NR, CL>(p, idx + 1, x.rank), H, t8);
     }
     ok = cross_sync(x, kXF, ni & 1, 38);
@@ -881,13 +917,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(x.bar(kFull + s), 1);
       mbar_init(x.bar(kEmpty + s), CL);
     }
+    for (int s = 0; s < C::kRSlots; ++s) {
+      mbar_init(x.bar(kRFull + s), 1);
+      mbar_init(x.bar(kREmpty + s), CL);
+    }
     for (int b = 0; b < 2; ++b) {
       mbar_init(x.bar(kSFull + b), 1);
       mbar_init(x.bar(kSFree + b), kSoftWarps);
       mbar_init(x.bar(kPFull + b), kSoftWarps);
       mbar_init(x.bar(kPFree + b), 1);
       mbar_init(x.bar(kXA + b), kSoftWarps);
-      mbar_init(x.bar(kXB + b), kSoftWarps);
     }
     mbar_init(x.bar(kQFull), 1);
     mbar_init(x.bar(kQFree), 1);
@@ -899,11 +938,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(x.bar(kDrainPV), 1);
     fence_barrier_init();
   }
-  if (x.tid <= kMaxSlots) reinterpret_cast<int*>(smem + kOffIssued)[x.tid] = -1;
+  if (x.tid <= kIssuedQ) reinterpret_cast<int*>(smem + kOffIssued)[x.tid] = -1;
   if (x.tid < 64) {
     // per-row state of the first item: reference and true maxima, causal end
-    reinterpret_cast<float*>(smem + kOffMref)[x.tid] = -INFINITY;
-    reinterpret_cast<float*>(smem + kOffMtrue)[x.tid] = -INFINITY;
+    for (int b = 0; b < 2; ++b) {
+      reinterpret_cast<float*>(smem + kOffMref)[b * 64 + x.tid] = -INFINITY;
+      reinterpret_cast<float*>(smem + kOffMtrue)[b * 64 + x.tid] = -INFINITY;
+    }
     if (x.it_begin < x.it_end)
       reinterpret_cast<int*>(smem + kOffVis)[x.tid] =
           visible_end(item_at<NR, CL>(p, x.it_begin, x.rank), p.num_heads, x.tid);
@@ -940,16 +981,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if constexpr (CL > 1) cluster_sync();
   if (x.tid == 0) {
     const volatile int* issued = reinterpret_cast<const volatile int*>(smem + kOffIssued);
-    for (int s = 0; s < C::kSlots; ++s) {
-      int last = issued[s];
+    for (int e = 0; e < kMaxSlots + kMaxRSlots; ++e) {
+      const bool rope = e >= kMaxSlots;
+      const int s = rope ? e - kMaxSlots : e;
+      if (s >= (rope ? C::kRSlots : C::kSlots)) continue;
+      int last = issued[e];
       if constexpr (CL > 1) {
-        const uint32_t rec = smem_u32(smem + kOffIssued + 4 * s);
+        const uint32_t rec = smem_u32(smem + kOffIssued + 4 * e);
         for (int r = 0; r < CL; ++r)
           if (r != x.rank) last = max(last, ld_cluster_s32(map_to_rank(rec, r)));
       }
-      if (last >= 0) drain_wait(x, x.bar(kFull + s), last & 1, 12);
+      if (last >= 0) drain_wait(x, x.bar(rope ? kRFull + s : kFull + s), last & 1, 12);
     }
-    if (issued[kMaxSlots] >= 0) drain_wait(x, x.bar(kQFull), issued[kMaxSlots] & 1, 13);
+    if (issued[kIssuedQ] >= 0) drain_wait(x, x.bar(kQFull), issued[kIssuedQ] & 1, 13);
   }
   // no CTA of the cluster exits while loads into another may still land
   if constexpr (CL > 1) cluster_sync();
@@ -1032,6 +1076,8 @@ cudaError_t launch_decode_hn(const DecodeParams& p, int rows, int cluster, int64
   cudaError_t e = make_row_map(&maps.q, p.q, static_cast<uint64_t>(q_rows), static_cast<uint32_t>(rows), true);
   if (e != cudaSuccess) return e;
   e = make_row_map(&maps.kv, p.kv, static_cast<uint64_t>(kv_rows), kHalf, true);
+  if (e != cudaSuccess) return e;
+  e = make_row_map(&maps.kvr, p.kv, static_cast<uint64_t>(kv_rows), kHalf, true, 64);
   if (e != cudaSuccess) return e;
   if (p.out != nullptr) {
     e = make_out_map(&maps.out, p.out, static_cast<uint64_t>(q_rows), 1, true);

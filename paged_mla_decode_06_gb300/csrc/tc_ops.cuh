@@ -340,6 +340,17 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// Same for a K-major operand in the 64-byte swizzle (8-row x 64-byte atoms,
+// sbo_bytes between 8-row groups).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t saddr, uint32_t sbo_bytes) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= 1ull << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= 1ull << 46;
+  d |= 4ull << 61;
+  return d;
+}
+
 // Shared-memory matrix descriptor without swizzling (8-row x 16-byte core
 // matrices). For an MN-major operand the leading-dimension byte offset is
 // the distance between core matrices adjacent in K (groups of 8 K indices)

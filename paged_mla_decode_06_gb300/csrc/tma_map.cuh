@@ -29,21 +29,21 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tma_encode_fn() {
 }
 
 // 2-D map over a [rows, 576] tensor of bf16 or e4m3 elements with boxes 128
-// bytes wide and box_rows rows high; reads past the last row or column fill
-// zeros.
+// bytes wide (or 64, with the 64-byte swizzle) and box_rows rows high; reads
+// past the last row or column fill zeros.
 inline cudaError_t make_row_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows,
-                                bool fp8) {
+                                bool fp8, uint32_t box_bytes = 128) {
   auto enc = tma_encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const uint32_t elt = fp8 ? 1 : 2;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(576), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(576) * elt};
-  cuuint32_t box[2] = {128 / elt, box_rows};
+  cuuint32_t box[2] = {box_bytes / elt, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   box_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
