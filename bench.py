@@ -133,8 +133,13 @@ PROFILED_TRAFFIC = {
     },
     (5, "fp8", 16): {  # decode_hn.cu, e4m3 batch at 16 heads (profiles/decode_hn_fp8.md)
         "source": "decode_hn.cu",
-        "code_sha256": "95e8a0df03df0c02955a6769a81b2005cd507b728945e8a4154701c0c84293d2",
-        "dram_per_alg_byte": (226.840576 + 3.565312) / 226.738272,
+        "code_sha256": "6dc1a0e376477084d95e203f130c7803da11a6b501982c01d9a77f70799d2fe9",
+        "dram_per_alg_byte": (226.829824 + 3.939840) / 226.738272,
+    },
+    (5, "fp8", 128): {  # decode_hn.cu on CTA-pair clusters, e4m3 batch at 128 heads (same file)
+        "source": "decode_hn.cu",
+        "code_sha256": "6dc1a0e376477084d95e203f130c7803da11a6b501982c01d9a77f70799d2fe9",
+        "dram_per_alg_byte": (228.408832 + 4.478464) / 228.286560,
     },
 }
 
@@ -710,7 +715,8 @@ def run_reference(args):
 def run_kernels_once():
     """One launch of every library kernel on inputs above the 129 MB L2, for
     a profiler's counter pass (no timing, no JSON line): the e4m3 decode at
-    128 heads (schedule, CTA-pair decode, merge), the sparse decode (index
+    128 heads (schedule, rows-as-N decode on CTA-pair clusters, merge; then
+    the CTA-pair kernel with the rows as M), the sparse decode (index
     conversion, schedule, decode, merge), the e4m3 decode at 16 heads on the
     warp-MMA kernel and on the rows-as-N kernel, the multi-token decode with
     sinks, the q concat/quantisation, the per-shard LSE merge, the sparse
@@ -727,6 +733,7 @@ def run_kernels_once():
     wm = I.fp8_decode(16, batch=16)
     wt = I.mtp_sinks(batch=16)                          # multi-token rows: 2-4 row tiles per request
     dwf = B.DeviceWorkload(wf, device=dev)
+    dwp = B.DeviceWorkload(wf, device=dev, kernel=B.MLA_KERNEL_TCGEN05)
     dws = B.DeviceWorkload(ws, device=dev)
     dwm = B.DeviceWorkload(wm, device=dev, kernel=B.MLA_KERNEL_WARP_MMA)
     dwn = B.DeviceWorkload(wm, device=dev)              # the rows-as-N kernel on the same batch
@@ -748,6 +755,7 @@ def run_kernels_once():
     fit = torch.empty(16384, 2048, dtype=torch.int32, device=dev)
     torch.cuda.synchronize()
     dwf.forward()
+    dwp.forward()
     dws.forward()
     dwm.forward()
     dwn.forward()
@@ -757,7 +765,7 @@ def run_kernels_once():
     B.mla_sparse_seqlen(qsl, seq, topk=2048, indptr=ptr)
     B.mla_fit_kpool_indices(ti, topk=2048, out=fit)
     torch.cuda.synchronize()
-    if any(d.status() != 0 for d in (dwf, dws, dwn, dwt)):
+    if any(d.status() != 0 for d in (dwf, dwp, dws, dwn, dwt)):
         raise RuntimeError("device status word set")
     print("kernels-once ok")
 
