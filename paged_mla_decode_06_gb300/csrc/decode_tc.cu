@@ -117,6 +117,8 @@ struct TcMaps {
   CUtensorMap q;     // q viewed as [T*H rows, 576], box 128 bytes x 128 rows
   CUtensorMap kv;    // cache viewed as [NB*BS rows, 576], box 128 bytes x 64 rows
   CUtensorMap kv1;   // sparse: the same view, box 128 bytes x 1 row (gather4)
+  CUtensorMap out;   // out as [T*H, 1, 512] bf16, box 32 rows x 64 columns, 128-byte swizzle
+  CUtensorMap part;  // partials as [slot rows, 1, 512] or [T*H, NS, 512] fp32, box 32 x 32
 };
 
 __device__ __forceinline__ void report(int* status, int code) {
@@ -682,7 +684,7 @@ __device__ void value_mma(const Ctx& x) {
 
 // ------------------------------------------------------------------ value CTA: rescale + epilogue
 template <bool FP8, bool SPARSE>
-__device__ void value_rows(const Ctx& x, const DecodeParams& p) {
+__device__ void value_rows(const Ctx& x, const TcMaps& maps, const DecodeParams& p) {
   using C = Cfg<FP8, SPARSE>;
   const int lane = x.lane;
   const int q4 = x.warp & 3;
@@ -753,14 +755,68 @@ __device__ void value_rows(const Ctx& x, const DecodeParams& p) {
     fence_after_sync();
   }
   if (ok) ok = __all_sync(0xffffffffu, wait_phase(x, x.bar(kFinal), 0, true, 55));
-  // Each warp scales its 32 rows and writes them out through its quarter of
-  // the last P slot (no P arrives after the last chunk), swizzled, so that
-  // every store instruction covers four 128-byte row pieces instead of 32
-  // scattered 16-byte pieces. TMEM loads are warp-collective (ok is
-  // warp-uniform).
+  // Each warp scales its 32 rows and stages them, 128 bytes of each row at a
+  // time, in its quarter of a P slot (no P arrives after the last chunk), in
+  // the 128-byte swizzle. When all 32 rows are valid one TMA tensor store
+  // writes each staged tile (two tiles in flight, one per P slot), so that
+  // the warp never waits on global stores. Otherwise every store
+  // instruction covers four 128-byte row pieces. TMEM loads are
+  // warp-collective (ok is warp-uniform).
   if (ok) {
     const float mult = reinterpret_cast<const float*>(x.smem + kOffMult)[r];
     uint8_t* stg = x.smem + C::kOffPRecv + ((n - 1) & 1) * kPBytes + q4 * 4096;
+    const bool whole = x.row0 + 32 * q4 + 32 <= x.rows_total && n > 0;
+    if (whole) {
+      // the warp's rows are consecutive rows of out, of the item's partial
+      // slot, or of the segment's partials
+      const int wr = x.row0 + 32 * q4;
+      const int z0 = x.fin || x.pslot < 0 ? x.tok0 * H + wr : x.pslot * kRows + 32 * q4;
+      const int y0 = x.fin || x.pslot >= 0 ? 0 : x.seg;
+      const CUtensorMap* map = x.fin ? &maps.out : &maps.part;
+      int staged = 0;
+      auto store = [&](const uint32_t (&w)[32], int col0) {
+        uint8_t* buf = x.smem + C::kOffPRecv + ((n - 1 + staged) & 1) * kPBytes + q4 * 4096;
+        if (staged >= 2) {  // the store that read this tile two passes ago
+          if (lane == 0) bulk_wait_read<1>();
+        }
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          *reinterpret_cast<uint4*>(buf + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+              make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(map, smem_u32(buf), col0, y0, z0);
+          bulk_commit_group();
+        }
+        ++staged;
+      };
+#pragma unroll 1
+      for (int g = 0; g < 8; ++g) {
+        uint32_t o[64];
+        tmem_ld_32x32b_x64(x.tbase + lane_off + kTmemO + 64 * g, o);
+        tmem_ld_wait();
+        if (x.fin) {
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            w[j] = pack_bf16(__uint_as_float(o[2 * j]) * mult, __uint_as_float(o[2 * j + 1]) * mult);
+          store(w, 64 * g);
+        } else {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t w[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(__uint_as_float(o[32 * hf + j]) * mult);
+            store(w, 64 * g + 32 * hf);
+          }
+        }
+      }
+      if (lane == 0) bulk_wait_all();  // tiles read and written before the CTA exits
+      __syncwarp();
+      return;
+    }
     const int qc = lane & 7;  // 16-byte piece of a 128-byte row piece
     // output bases (16-byte units) of the 8 rows this lane writes, rows
     // 4 * it + lane / 8 of the warp's 32; null past the last valid row
@@ -1027,7 +1083,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
     if (x.warp == 1) {
       value_mma<FP8, SPARSE>(x);
     } else if (x.warp >= 2 && x.warp < 6) {
-      value_rows<FP8, SPARSE>(x, p);
+      value_rows<FP8, SPARSE>(x, maps, p);
     } else if constexpr (SPARSE) {
       if (x.warp >= 6) value_stage_gather<SPARSE>(x, maps, p, x.warp - 6);
     } else if constexpr (FP8) {
@@ -1094,6 +1150,17 @@ cudaError_t launch_decode_tc(const DecodeParams& p, bool fp8, int64_t q_rows, in
   if (e != cudaSuccess) return e;
   e = make_row_map(&maps.kv, p.kv, static_cast<uint64_t>(kv_rows), kKeys, fp8);
   if (e != cudaSuccess) return e;
+  if (p.out != nullptr) {
+    e = make_out_map(&maps.out, p.out, static_cast<uint64_t>(q_rows), 1, true, 64, 32, true);
+    if (e != cudaSuccess) return e;
+  }
+  if (p.segm_out != nullptr) {
+    e = p.items != nullptr
+            ? make_out_map(&maps.part, p.segm_out, static_cast<uint64_t>(p.segm_rows), 1, false, 32, 32, true)
+            : make_out_map(&maps.part, p.segm_out, static_cast<uint64_t>(q_rows),
+                           static_cast<uint64_t>(p.num_segments), false, 32, 32, true);
+    if (e != cudaSuccess) return e;
+  }
   if (p.slots != nullptr) {
     if (fp8) return cudaErrorNotSupported;
     e = make_row_map(&maps.kv1, p.kv, static_cast<uint64_t>(kv_rows), 1, false);

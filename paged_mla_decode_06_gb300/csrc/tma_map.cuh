@@ -48,20 +48,23 @@ inline cudaError_t make_row_map(CUtensorMap* m, const void* base, uint64_t rows,
 }
 
 // 3-D map over an output tensor [rows, mid, 512] of fp32 (or bf16 with
-// `bf16`) values, row stride mid * 512 elements, for stores of 8-row x
-// 32-column boxes (one box column at a time along `mid`), no swizzle.
-inline cudaError_t make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t mid, bool bf16) {
+// `bf16`) values, row stride mid * 512 elements, for stores of boxes of
+// box_rows rows x box_cols columns (one box column at a time along `mid`):
+// by default 8 x 32 without swizzle; with `sw128` the shared-memory tile is
+// in the 128-byte swizzle (box_cols x element size must then be 128 bytes).
+inline cudaError_t make_out_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t mid, bool bf16,
+                                uint32_t box_cols = 32, uint32_t box_rows = 8, bool sw128 = false) {
   auto enc = tma_encode_fn();
   if (enc == nullptr) return cudaErrorNotSupported;
   const uint64_t elt = bf16 ? 2 : 4;
   cuuint64_t dims[3] = {static_cast<cuuint64_t>(512), static_cast<cuuint64_t>(mid), static_cast<cuuint64_t>(rows)};
   cuuint64_t strides[2] = {static_cast<cuuint64_t>(512 * elt), static_cast<cuuint64_t>(512 * elt * mid)};
-  cuuint32_t box[3] = {32, 1, 8};
+  cuuint32_t box[3] = {box_cols, 1, box_rows};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   sw128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
