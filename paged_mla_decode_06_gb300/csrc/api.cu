@@ -156,6 +156,13 @@ dim3 grid_of(const mla_plan_t* plan) {
               static_cast<unsigned>(plan->grid_z));
 }
 
+// Workers of a balanced plan: split_items = 2 x workers partial slots (2 x
+// workers x row tiles for the CTA pair, whose units' cuts split every tile).
+int32_t plan_workers(const mla_plan_t* plan) {
+  const int32_t per_cut = plan->kernel == mla::kTcPair128 && plan->row_tiles > 0 ? plan->row_tiles : 1;
+  return plan->split_items / (2 * per_cut);
+}
+
 // Workspace pieces of the balanced schedule (after the status block):
 // the item count, the items (32 bytes each), the unit table, each worker's
 // first item (rows-as-N kernel), then the partial slots at the plan's
@@ -172,7 +179,7 @@ SchedLayout sched_layout(const mla_plan_t* plan) {
   l.items = 2 * kWsAlign;
   l.unit_tab = l.items + align_up(static_cast<size_t>(plan->max_items) * 32, kWsAlign);
   l.worker_first = l.unit_tab + align_up(units * static_cast<size_t>(plan->row_tiles) * 8, kWsAlign);
-  l.end = l.worker_first + align_up((static_cast<size_t>(plan->split_items) / 2 + 1) * 4, kWsAlign);
+  l.end = l.worker_first + align_up((static_cast<size_t>(plan_workers(plan)) + 1) * 4, kWsAlign);
   return l;
 }
 
@@ -192,7 +199,7 @@ mla_status_t launch_decode(const mla_plan_t* plan, const mla::DecodeParams& d, i
   }
   if (plan->kernel == mla::kTcRowsN) {
     const int cluster = plan->tile_rows / plan->rows_per_cta;
-    const unsigned workers = static_cast<unsigned>(plan->split_items / 2);
+    const unsigned workers = static_cast<unsigned>(plan_workers(plan));
     const dim3 grid = d.items != nullptr ? dim3(workers * cluster, 1u, 1u) : grid_of(plan);
     return cuda_status(mla::launch_decode_hn(d, plan->rows_per_cta, cluster, q_rows, kv_rows, grid,
                                              status, stream));
@@ -220,10 +227,9 @@ mla::SchedParams sched_params(const mla_plan_t* plan, const Inputs& in, uint8_t*
   sp.items = reinterpret_cast<int32_t*>(ws + l.items);
   sp.n_items = reinterpret_cast<int32_t*>(ws + l.n_items);
   sp.unit_tab = reinterpret_cast<int32_t*>(ws + l.unit_tab);
-  if (plan->kernel == mla::kTcRowsN) {  // workers run contiguous runs of items
+  sp.workers = plan_workers(plan);
+  if (plan->kernel == mla::kTcRowsN)  // workers run contiguous runs of items
     sp.worker_first = reinterpret_cast<int32_t*>(ws + l.worker_first);
-    sp.workers = plan->split_items / 2;
-  }
   return sp;
 }
 
@@ -231,7 +237,7 @@ mla_status_t check_scheduled(const mla_plan_t* plan, const void* workspace, size
   if (plan == nullptr || plan->schedule != 1) return MLA_ERR_INVALID_ARG;
   if ((plan->kernel != mla::kTcPair128 && plan->kernel != mla::kTcRowsN) || plan->max_items <= 0 ||
       plan->split_items <= 0 || plan->row_tiles <= 0 || plan->rows_per_cta <= 0 ||
-      plan->tile_rows < plan->rows_per_cta || plan->split_items / 2 > kMaxWorkers)
+      plan->tile_rows < plan->rows_per_cta || plan_workers(plan) > kMaxWorkers || plan_workers(plan) < 1)
     return MLA_ERR_INVALID_ARG;
   if (workspace == nullptr || workspace_bytes < plan->workspace_bytes) return MLA_ERR_WORKSPACE;
   if (!aligned(workspace, kWsAlign)) return MLA_ERR_INVALID_ARG;
@@ -402,10 +408,13 @@ mla_status_t mla_decode_plan(const mla_problem_t* prob, mla_plan_t* plan) {
     }
     if (workers < 1) workers = 1;
     if (workers > kMaxWorkers) workers = kMaxWorkers;
-    const int32_t split_cap = 2 * workers;
+    // the CTA pair cuts a unit of several row tiles once for all of them:
+    // each cut then splits every tile (sched.cu)
+    const int32_t per_cut = use_pair ? row_tiles : 1;
+    const int32_t split_cap = 2 * workers * per_cut;
     plan->schedule = 1;
     plan->split_items = split_cap;
-    plan->max_items = static_cast<int32_t>(unit_tiles + workers);  // rows + cuts
+    plan->max_items = static_cast<int32_t>(unit_tiles + static_cast<int64_t>(workers) * per_cut);  // rows + cuts
     const SchedLayout l = sched_layout(plan);
     const size_t slot_rows = static_cast<size_t>(split_cap) * tile_rows;
     const size_t out_b = align_up(slot_rows * kRank * sizeof(float), kWsAlign);

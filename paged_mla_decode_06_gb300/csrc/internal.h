@@ -65,7 +65,7 @@ struct SchedParams {
   // multiple of cdiv(total, workers) groups, worker w's first item at
   // worker_first[w] ([workers + 1]); else longest first for one-item CTAs
   int32_t* worker_first;
-  int32_t workers;
+  int32_t workers;               // the share of the groups is cdiv(total, workers)
 };
 
 cudaError_t launch_schedule(const SchedParams& p, cudaStream_t stream);

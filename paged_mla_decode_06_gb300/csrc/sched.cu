@@ -22,6 +22,13 @@
 // count, from which the merge finds them. Cuts number
 // fewer than the workers, so the slots of split rows number at most two per
 // worker and the items at most rows + workers.
+// A unit of T > 1 row tiles (multi-token requests on the CTA pair) is cut
+// once for all its tiles: the sequence is that of the units' g groups (W
+// still the worker's share of all tiles' groups), so that the tiles' items
+// cover the same keys. They are written next to each other, and their pairs
+// read the keys together (one HBM pass, the other tiles hitting L2). Split
+// units then own T k slots: at most 2 T_max per worker, and the items are at
+// most rows + T_max workers. With one tile per unit this is the rule above.
 //
 // Contiguous mode (the rows-as-N kernel, whose workers run many items each):
 // every multiple of W inside a row is a cut, so that worker w's share is
@@ -108,7 +115,7 @@ struct Cuts {
 };
 
 template <typename I>
-__device__ __forceinline__ Cuts<I> row_cuts(I a, int g, I W, bool every = false) {
+__device__ __forceinline__ Cuts<I> row_cuts(I a, I g, I W, bool every = false) {
   const I d = every ? 0 : W / 8;
   const I lo = a + d + 1, hi = a + g - d - 1;  // allowed cut positions
   Cuts<I> c{0, 0};
@@ -119,12 +126,30 @@ __device__ __forceinline__ Cuts<I> row_cuts(I a, int g, I W, bool every = false)
   return c;
 }
 
-// The histogram, the ranking and the items, with positions of type I.
+// Piece boundaries of a unit of g key groups at position a of the sequence
+// of the units' groups: the multiples of W inside [a, a + g), none within
+// W / 8 of its ends, as group offsets. All of the unit's row tiles are cut
+// there. f(b) is called for each boundary in increasing order; returns
+// their number.
+template <typename I, typename F>
+__device__ int unit_bounds(I a, int g, int T, I W, F f) {
+  if (g <= 1 || T <= 0) return 0;
+  const Cuts<I> c = row_cuts<I>(a, static_cast<I>(g), W);
+  for (int j = 0; j < c.count; ++j) f(static_cast<int>(c.first + static_cast<I>(j) * W - a));
+  return c.count;
+}
+
+// The histogram, the ranking and the items, with positions of type I. The
+// T items of a piece (one per row tile) are written next to each other, so
+// that the CTA pairs that read the same keys start together and the keys
+// come from HBM once, the other tiles' reads hitting L2.
 template <typename I, typename Info>
 __device__ void schedule_items(const SchedParams& p, Info info, I W, long long* red, int* hist, int* start) {
   const int tid = threadIdx.x;
   const int U = p.num_units;
-  // piece-size histogram; rows of unit u start at pos_u (unit-major)
+  auto bin_of = [](long long size) { return static_cast<int>(min(size, static_cast<long long>(kSizeBins - 1))); };
+  // piece-size histogram (T items per piece); unit u starts at pos_u of
+  // the sequence of the units' groups
   for (int b = tid; b < kSizeBins; b += kThreads) hist[b] = 0;
   I carry = 0;
   for (int u0 = 0; u0 < U; u0 += kThreads) {
@@ -132,18 +157,15 @@ __device__ void schedule_items(const SchedParams& p, Info info, I W, long long* 
     UnitInfo i{0, 0};
     if (u < U) i = info(u);
     I sum;
-    const I pos = carry + block_exclusive_scan<I>(static_cast<I>(i.tiles) * i.groups, red, &sum);
+    const I pos = carry + block_exclusive_scan<I>(static_cast<I>(i.groups), red, &sum);
     carry += sum;
-    for (int t = 0; t < i.tiles; ++t) {
-      const I a = pos + static_cast<I>(t) * i.groups;
-      const Cuts<I> c = row_cuts<I>(a, i.groups, W);
-      I prev = a;
-      for (int j = 0; j <= c.count; ++j) {
-        const I next = j < c.count ? c.first + j * W : a + i.groups;
-        atomicAdd(&hist[static_cast<int>(min(static_cast<long long>(next - prev),
-                                             static_cast<long long>(kSizeBins - 1)))], 1);
-        prev = next;
-      }
+    if (i.tiles > 0) {
+      int prev = 0;
+      unit_bounds<I>(pos, i.groups, i.tiles, W, [&](int b) {
+        atomicAdd(&hist[bin_of(b - prev)], i.tiles);
+        prev = b;
+      });
+      atomicAdd(&hist[bin_of(i.groups - prev)], i.tiles);
     }
   }
   __syncthreads();
@@ -167,7 +189,7 @@ __device__ void schedule_items(const SchedParams& p, Info info, I W, long long* 
   for (int b = tid; b < kSizeBins; b += kThreads) hist[b] = 0;  // now the per-bin cursor
   __syncthreads();
 
-  // items, unit table and partial slots (slots of split rows, row order)
+  // items, unit table and partial slots (k per row tile of a split unit, tile-major)
   carry = 0;
   int slot_carry = 0;
   long long n_items = 0;
@@ -176,38 +198,34 @@ __device__ void schedule_items(const SchedParams& p, Info info, I W, long long* 
     UnitInfo i{0, 0};
     if (u < U) i = info(u);
     I sum;
-    const I pos = carry + block_exclusive_scan<I>(static_cast<I>(i.tiles) * i.groups, red, &sum);
+    const I pos = carry + block_exclusive_scan<I>(static_cast<I>(i.groups), red, &sum);
     carry += sum;
-    int nslots = 0;
-    for (int t = 0; t < i.tiles; ++t) {
-      const Cuts<I> c = row_cuts<I>(pos + static_cast<I>(t) * i.groups, i.groups, W);
-      if (c.count > 0) nslots += c.count + 1;
-    }
+    const int k = i.tiles > 0 ? unit_bounds<I>(pos, i.groups, i.tiles, W, [](int) {}) + 1 : 0;
+    const int nslots = k > 1 ? k * i.tiles : 0;
     int slot_sum;
-    int slot = slot_carry + block_exclusive_scan<int>(nslots, red, &slot_sum);
+    const int slot = slot_carry + block_exclusive_scan<int>(nslots, red, &slot_sum);
     slot_carry += slot_sum;
-    for (int t = 0; t < i.tiles; ++t) {
-      const I a = pos + static_cast<I>(t) * i.groups;
-      const Cuts<I> c = row_cuts<I>(a, i.groups, W);
-      const int k = c.count + 1;
-      const int pbase = k > 1 ? slot : -1;
-      reinterpret_cast<int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + t] = make_int2(pbase, k);
-      I prev = a;
-      for (int j = 0; j < k; ++j) {
-        const I next = j < c.count ? c.first + j * W : a + i.groups;
-        const int bin = static_cast<int>(min(static_cast<long long>(next - prev),
-                                             static_cast<long long>(kSizeBins - 1)));
-        const int at = start[bin] + atomicAdd(&hist[bin], 1);
-        int4* it = reinterpret_cast<int4*>(p.items) + 2 * static_cast<int64_t>(at);
-        const long long kb = static_cast<long long>(prev - a) * kGroupKeys;
-        const long long ke = static_cast<long long>(next - a) * kGroupKeys;
-        it[0] = make_int4(u, t, static_cast<int>(min(kb, static_cast<long long>(INT32_MAX))),
-                          static_cast<int>(min(ke, static_cast<long long>(INT32_MAX))));
-        it[1] = make_int4(k > 1 ? pbase + j : -1, 0, 0, 0);
-        prev = next;
-      }
-      n_items += k;
-      if (k > 1) slot += k;
+    if (i.tiles > 0) {
+      for (int t = 0; t < i.tiles; ++t)
+        reinterpret_cast<int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + t] =
+            make_int2(k > 1 ? slot + t * k : -1, k);
+      int prev = 0, j = 0;
+      auto emit = [&](int b) {
+        const int at = start[bin_of(b - prev)] + atomicAdd(&hist[bin_of(b - prev)], i.tiles);
+        const long long kb = static_cast<long long>(prev) * kGroupKeys;
+        const long long ke = static_cast<long long>(b) * kGroupKeys;
+        for (int t = 0; t < i.tiles; ++t) {
+          int4* it = reinterpret_cast<int4*>(p.items) + 2 * static_cast<int64_t>(at + t);
+          it[0] = make_int4(u, t, static_cast<int>(min(kb, static_cast<long long>(INT32_MAX))),
+                            static_cast<int>(min(ke, static_cast<long long>(INT32_MAX))));
+          it[1] = make_int4(k > 1 ? slot + t * k + j : -1, 0, 0, 0);
+        }
+        prev = b;
+        ++j;
+      };
+      unit_bounds<I>(pos, i.groups, i.tiles, W, emit);
+      emit(i.groups);
+      n_items += static_cast<long long>(k) * i.tiles;
     }
   }
   n_items = block_sum(n_items, red);
@@ -316,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams
       schedule_contiguous<long long>(p, info, W, workers, red, hist);
     return;
   }
-  const long long workers = p.split_cap / 2 > 0 ? p.split_cap / 2 : 1;
+  const long long workers = p.workers > 0 ? p.workers : 1;
   const long long W = total > 0 ? (total + workers - 1) / workers : 1;
   if (total < (1ll << 30))
     schedule_items<int>(p, info, static_cast<int>(W), red, hist, start);

@@ -402,8 +402,9 @@ def test_plan_random_problems_are_consistent(lib):
             assert plan.kernel in (4, 5) and ns == 0 and plan.num_segments == 1
             pairs = plan.kernel == 4 or plan.tile_rows > plan.rows_per_cta
             workers = min(1024, max(1, sms // 2) if pairs else sms)
-            assert plan.split_items == 2 * workers
-            assert plan.max_items == units * plan.row_tiles + workers
+            per_cut = plan.row_tiles if plan.kernel == 4 else 1  # a cut splits every tile of a unit
+            assert plan.split_items == 2 * workers * per_cut
+            assert plan.max_items == units * plan.row_tiles + workers * per_cut
             rows = plan.split_items * plan.tile_rows
             assert plan.segm_output_offset >= 512 + plan.max_items * 32
             assert plan.segm_max_offset >= plan.segm_output_offset + rows * 512 * 4

@@ -15,6 +15,7 @@ from paged_mla_decode_06_gb300 import binding as B
 from paged_mla_decode_06_gb300 import build as BUILD
 from paged_mla_decode_06_gb300 import inputs as I
 from tests.gpu_helpers import assert_close, oracle_slots, run_gpu, run_oracle, visible_keys
+from tests.test_schedule_rule import cut_rule
 
 pytestmark = pytest.mark.gpu
 
@@ -196,7 +197,9 @@ def test_balanced_schedule_items(case):
     the pieces of every (unit, row tile) cover its key groups once and in
     order, items come longest first, split pieces own distinct partial slots
     within the budget, the items fit the grid, the output matches the oracle,
-    and a second decode and merge over the same list give the same bits."""
+    and a second decode and merge over the same list give the same bits.
+    The pieces equal the cut rule's (host model), and the row tiles of a
+    multi-token request are cut at the same keys and listed side by side."""
     if case == "dense":
         w = I.build_dense(71, seq_lens=[0, 1, 129, 700, 3000, 9000, 257], num_heads=128,
                           block_size=64, num_segments=0)
@@ -242,6 +245,22 @@ def test_balanced_schedule_items(case):
             else:
                 assert mine[0, 4] == -1 and tab[u, t, 0] == -1
     assert n == sum(max(1, int(tab[u, t, 1])) for u in range(len(lens)) for t in range(int(tiles[u])))
+    # the host model of the rule gives the same pieces, row by row
+    groups = [-(-int(x) // 128) for x in lens]
+    per_cut = plan.row_tiles
+    rows_m, pieces_m, _ = cut_rule(groups, [int(t) for t in tiles], plan.split_items // (2 * per_cut))
+    r = 0
+    for u in range(len(lens)):
+        for t in range(int(tiles[u])):
+            mine = items[(items[:, 0] == u) & (items[:, 1] == t)]
+            mine = mine[np.argsort(mine[:, 2])]
+            assert ((mine[:, 3] - mine[:, 2]) // 128).tolist() == pieces_m[r], (u, t)
+            r += 1
+    # a piece's row tiles are consecutive items
+    for i in range(n):
+        u, t, kb = items[i, 0], items[i, 1], items[i, 2]
+        if t > 0:
+            assert items[i - 1, 0] == u and items[i - 1, 1] == t - 1 and items[i - 1, 2] == kb
     assert len(set(slots)) == len(slots) and all(0 <= s < plan.split_items for s in slots)
     assert n <= plan.max_items
     assert split or case == "sparse" or n == sum(int(t) for t in tiles)

@@ -13,23 +13,30 @@ import pytest
 
 
 def cut_rule(groups, tiles, pairs):
-    rows = [g for g, t in zip(groups, tiles) for _ in range(t)]
-    total = sum(rows)
+    """The CTA pair's rule. W is a worker's share of all row tiles' groups;
+    the units' g groups are laid end to end and cut at the multiples of W
+    inside each unit, none within W / 8 of its ends; all T row tiles of a
+    unit are cut there. Returns the rows (one per tile), each row's piece
+    sizes, and W."""
+    total = sum(g * t for g, t in zip(groups, tiles))
     W = -(-total // pairs) if total > 0 else 1
     d = W // 8
-    pieces, pos = [], 0
-    for g in rows:
-        a, b = pos, pos + g
-        lo, hi = a + d + 1, b - d - 1
-        cuts = []
-        if g > 0 and hi >= lo:
+    rows, pieces, pos = [], [], 0
+    for g, t in zip(groups, tiles):
+        a = pos
+        lo, hi = a + d + 1, a + g - d - 1
+        bounds = []
+        if g > 1 and hi >= lo and t > 0:
             c = -(-lo // W) * W
             while c <= hi:
-                cuts.append(c)
+                bounds.append(c - a)
                 c += W
-        bounds = [a] + cuts + [b]
-        pieces.append([bounds[i + 1] - bounds[i] for i in range(len(bounds) - 1)])
-        pos = b
+        edges = [0] + bounds + [g]
+        sizes = [edges[i + 1] - edges[i] for i in range(len(edges) - 1)]
+        for _ in range(t):
+            rows.append(g)
+            pieces.append(list(sizes))
+        pos += g
     return rows, pieces, W
 
 
@@ -52,15 +59,23 @@ def test_cut_rule_stays_inside_the_workspace(name, pairs):
     else:
         groups, tiles = CASES[name]
     rows, pieces, W = cut_rule(groups, tiles, pairs)
+    tmax = max(tiles)
     n_items = sum(len(p) for p in pieces)
     slots = sum(len(p) for p in pieces if len(p) > 1)
-    assert n_items <= len(rows) + pairs            # plan: max_items = rows + pairs
-    assert slots <= 2 * pairs                      # plan: split_items = 2 * pairs slots
+    assert n_items <= len(rows) + tmax * pairs     # plan: max_items = rows + T_max * pairs
+    assert slots <= 2 * tmax * pairs               # plan: split_items = 2 * T_max * pairs slots
     for g, p in zip(rows, pieces):
         assert sum(p) == g and all(x >= 0 for x in p)  # each row covered once
-        if len(p) > 1:                             # no sliver next to a row's ends
+    # no sliver next to a row's ends, no piece above W; every tile of a unit
+    # cut at the same keys
+    r = 0
+    for g, t in zip(groups, tiles):
+        p = pieces[r]
+        assert all(pieces[r + k] == p for k in range(t))
+        if len(p) > 1:
             assert p[0] > W // 8 and p[-1] > W // 8
             assert all(x <= W for x in p[1:-1])
+        r += t
 
 
 def contiguous_rule(groups, tiles, workers):
