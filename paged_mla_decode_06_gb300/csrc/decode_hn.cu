@@ -896,7 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   x.rank = CL > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   if (p.items != nullptr) {
     // balanced schedule: this worker's items, once the grid that wrote the
-    // list (launched just before) has completed
+    // list has completed (a no-op unless launched as its programmatic dependent)
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     // the merge grid may launch once every CTA of this one has started
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
@@ -1036,12 +1036,9 @@ cudaError_t launch_rows(const HnMaps& maps, const DecodeParams& p, dim3 grid, in
     attr[n].val.clusterDim.z = 1;
     ++n;
   }
-  if (p.items != nullptr) {
-    // balanced schedule: programmatic dependent launch after the schedule kernel
-    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[n].val.programmaticStreamSerializationAllowed = 1;
-    ++n;
-  }
+  // an ordinary launch after the schedule kernel: as a programmatic dependent
+  // of it the 16-head e4m3 call measured 114.7 us against 110.6 us (the
+  // kernel's griddepcontrol.wait is then a no-op)
   cfg.attrs = attr;
   cfg.numAttrs = n;
   return cudaLaunchKernelEx(&cfg, decode_hn_kernel<NR, CL>, maps, p, status);

@@ -951,7 +951,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<FP8, SPARSE>::kT
   x.pslot = -1;
   if (p.items != nullptr) {
     // balanced schedule: both CTAs of the pair read the same item, once the
-    // grid that wrote the list (launched just before) has completed
+    // grid that wrote the list has completed (a no-op unless this grid was
+    // launched as a programmatic dependent of it)
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     // the merge grid may launch once every CTA of this one has started (it
     // waits for this grid to complete before it reads)
@@ -1118,23 +1119,11 @@ cudaError_t launch_variant(const TcMaps& maps, const DecodeParams& p, dim3 grid,
     if (e != cudaSuccess) return e;
     done.fetch_or(bit, std::memory_order_acq_rel);
   }
-  if (p.items == nullptr) {
-    decode_tc_kernel<FP8, SPARSE><<<grid, C::kThreads, C::kSmem, stream>>>(maps, p, status);
-    return cudaGetLastError();
-  }
-  // balanced schedule: programmatic dependent launch, so that the grid is
-  // set up while the schedule kernel before it runs
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = grid;
-  cfg.blockDim = dim3(C::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<FP8, SPARSE>, maps, p, status);
+  // an ordinary launch also after the schedule kernel: as a programmatic
+  // dependent of it (set up while it runs) the DeepSeek-V3 call measured
+  // 137.8 us against 131.0 us (its griddepcontrol.wait is then a no-op)
+  decode_tc_kernel<FP8, SPARSE><<<grid, C::kThreads, C::kSmem, stream>>>(maps, p, status);
+  return cudaGetLastError();
 }
 
 }  // namespace
