@@ -24,10 +24,15 @@ def _lib():
     B.load_library()
 
 
-def test_bounded_wait_runs_out_and_is_reported():
-    w = I.fp8_decode(16, batch=4, seq_len=4096)
+@pytest.mark.parametrize("heads", [16, 128])
+def test_bounded_wait_runs_out_and_is_reported(heads):
+    """16 heads: one CTA per worker; 128 heads: clusters of two CTAs whose
+    key boxes are multicast, where a CTA that gives up must still drain every
+    box its peer armed on it before either exits."""
+    w = I.fp8_decode(heads, batch=4, seq_len=4096)
     dw = B.DeviceWorkload(w)
     assert dw.plan.kernel == 5  # the rows-as-N kernel, balanced schedule
+    assert dw.plan.tile_rows == (2 if heads > 64 else 1) * dw.plan.rows_per_cta
     assert B.mla_workspace_status(dw.plan, dw.workspace) == 0
     dw.plan.wait_limit_us = 1
     dw.forward()                # returns: the kernel gives up and exits
@@ -52,3 +57,25 @@ def test_bounded_wait_runs_out_and_is_reported():
     assert B.mla_workspace_status(dw.plan, dw.workspace) == 0
     assert_close(dw.out.float().cpu().numpy()[tokens], dw.lse.cpu().numpy()[tokens],
                  ref_o, ref_l, "fp8", "cleared workspace")
+
+
+def test_bounded_wait_runs_out_on_the_cta_pair():
+    """The CTA-pair kernel (bf16, balanced schedule): with a 1 microsecond
+    limit the score and value CTAs give up, drain their copies to each other
+    and their MMAs, and exit; the next call with the default limit decodes
+    correctly."""
+    w = I.build_dense(91, seq_lens=[3000, 700, 129, 4100], num_heads=128, block_size=64, num_segments=0)
+    dw = B.DeviceWorkload(w, kernel=B.MLA_KERNEL_TCGEN05)
+    assert dw.plan.kernel == 4 and dw.plan.schedule == 1
+    dw.plan.wait_limit_us = 1
+    dw.forward()
+    torch.cuda.synchronize()
+    code = B.mla_workspace_status(dw.plan, dw.workspace, clear=True)
+    assert code != 0
+    dw.plan.wait_limit_us = 0
+    dw.forward()
+    torch.cuda.synchronize()
+    assert B.mla_workspace_status(dw.plan, dw.workspace) == 0
+    ref_o, ref_l = run_oracle(w)
+    assert_close(dw.out.float().cpu().numpy(), dw.lse.cpu().numpy(), ref_o, ref_l, "bf16",
+                 "CTA pair after a timed-out call")
