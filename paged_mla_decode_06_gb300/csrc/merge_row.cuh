@@ -44,6 +44,17 @@ __device__ void merge_row(const float* segm_out, const float* segm_max, const fl
     lk[u] = u < live ? merge_load_f<Coherent>(segm_expsum + base + u * stride) : 0.f;
     mk[u] = u < live ? merge_load_f<Coherent>(segm_max + base + u * stride) : -INFINITY;
   }
+  // the outputs of the first four partials are loaded with no wait for their
+  // weights (one memory round trip instead of two); a partial that carries
+  // no mass (possibly never written: stale or NaN) is excluded by select
+  float4 x0[4][VPL];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float4* src = reinterpret_cast<const float4*>(segm_out + (base + u * stride) * (VPL * 128));
+#pragma unroll
+    for (int v = 0; v < VPL; ++v)
+      x0[u][v] = u < live ? merge_load<Coherent>(src + v * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   float M = sink2;
 #pragma unroll
   for (int u = 0; u < kMeta; ++u)
@@ -52,6 +63,10 @@ __device__ void merge_row(const float* segm_out, const float* segm_max, const fl
     const int64_t i = base + s * stride;
     if (merge_load_f<Coherent>(segm_expsum + i) > 0.f) M = fmaxf(M, merge_load_f<Coherent>(segm_max + i));
   }
+  float acc[VPL][4];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
+  float W = 0.f;
   if (M == -INFINITY) {
 #pragma unroll
     for (int v = 0; v < VPL; ++v)
@@ -59,27 +74,38 @@ __device__ void merge_row(const float* segm_out, const float* segm_max, const fl
     if (lane == 0) *lse = -INFINITY;
     return;
   }
-  float acc[VPL][4];
+  // weight of partial s (its (max, expsum) pair from the first kMeta kept in
+  // registers, else loaded)
+  auto weight = [&](int s) {
+    float l = 0.f, m = 0.f;
+    if (s < kMeta) {
 #pragma unroll
-  for (int v = 0; v < VPL; ++v) acc[v][0] = acc[v][1] = acc[v][2] = acc[v][3] = 0.f;
-  float W = 0.f;
-  for (int s0 = 0; s0 < live; s0 += 4) {
+      for (int k = 0; k < kMeta; ++k)
+        if (k == s) { l = lk[k]; m = mk[k]; }
+    } else if (s < live) {
+      l = merge_load_f<Coherent>(segm_expsum + base + s * stride);
+      m = merge_load_f<Coherent>(segm_max + base + s * stride);
+    }
+    return l > 0.f ? l * exp2f(m - M) : 0.f;
+  };
+  auto add = [&](float wu, const float4 (&xu)[VPL]) {
+    W += wu;
+    if (wu != 0.f) {
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        acc[v][0] += wu * xu[v].x;
+        acc[v][1] += wu * xu[v].y;
+        acc[v][2] += wu * xu[v].z;
+        acc[v][3] += wu * xu[v].w;
+      }
+    }
+  };
+#pragma unroll
+  for (int u = 0; u < 4; ++u) add(weight(u), x0[u]);
+  for (int s0 = 4; s0 < live; s0 += 4) {
     float w[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int s = s0 + u;
-      float l = 0.f, m = 0.f;
-      if (s < kMeta) {
-#pragma unroll
-        for (int k = 0; k < kMeta; ++k)
-          if (k == s) { l = lk[k]; m = mk[k]; }
-      } else if (s < live) {
-        l = merge_load_f<Coherent>(segm_expsum + base + s * stride);
-        m = merge_load_f<Coherent>(segm_max + base + s * stride);
-      }
-      w[u] = l > 0.f ? l * exp2f(m - M) : 0.f;
-      W += w[u];
-    }
+    for (int u = 0; u < 4; ++u) w[u] = weight(s0 + u);
     float4 x[4][VPL];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -89,14 +115,7 @@ __device__ void merge_row(const float* segm_out, const float* segm_max, const fl
         x[u][v] = w[u] != 0.f ? merge_load<Coherent>(src + v * 32 + lane) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int v = 0; v < VPL; ++v) {
-        acc[v][0] += w[u] * x[u][v].x;
-        acc[v][1] += w[u] * x[u][v].y;
-        acc[v][2] += w[u] * x[u][v].z;
-        acc[v][3] += w[u] * x[u][v].w;
-      }
+    for (int u = 0; u < 4; ++u) add(w[u], x[u]);
   }
   if (sink2 != -INFINITY) W += exp2f(sink2 - M);
   const float inv = 1.f / W;
