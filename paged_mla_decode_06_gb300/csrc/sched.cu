@@ -232,6 +232,134 @@ __device__ void schedule_items(const SchedParams& p, Info info, I W, long long* 
   if (tid == 0) *p.n_items = static_cast<int32_t>(n_items);
 }
 
+// Exclusive prefixes of three per-thread counts over the block (thread
+// order) and their totals.
+__device__ int3 block_exclusive_scan3(int3 v, int3* red3, int3* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int3 inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, inc.x, o);
+    const int b = __shfl_up_sync(0xffffffffu, inc.y, o);
+    const int c = __shfl_up_sync(0xffffffffu, inc.z, o);
+    if (lane >= o) {
+      inc.x += a;
+      inc.y += b;
+      inc.z += c;
+    }
+  }
+  __syncthreads();
+  if (lane == 31) red3[warp] = inc;
+  __syncthreads();
+  int3 before = make_int3(0, 0, 0), all = make_int3(0, 0, 0);
+#pragma unroll 1
+  for (int w = 0; w < kThreads / 32; ++w) {
+    const int3 r = red3[w];
+    if (w < warp) {
+      before.x += r.x;
+      before.y += r.y;
+      before.z += r.z;
+    }
+    all.x += r.x;
+    all.y += r.y;
+    all.z += r.z;
+  }
+  *total = all;
+  return make_int3(before.x + inc.x - v.x, before.y + inc.y - v.y, before.z + inc.z - v.z);
+}
+
+// The longest-first list when the units fit one per thread and their pieces
+// fit kSmallPieces: each piece's place is counted directly (the items of
+// the pieces larger than it, or as large and earlier in unit order), so the
+// list is the same on every run and the kernel runs a few short phases (it
+// is on the call's critical path, mostly waiting for its own code to load).
+// Same pieces, slots and unit table as schedule_items. Returns false, having
+// written nothing, when the pieces do not fit.
+constexpr int kSmallPieces = 512;
+static_assert(kSmallPieces <= 4096, "order keys hold the list position in 12 bits");
+
+// Order key of piece q of the small list: its size in groups (clamped to 19
+// bits: pieces that long are in any order among themselves), then its list
+// position q < 4096 (earlier first). Distinct for distinct q.
+__device__ __forceinline__ int order_key(int size, int q) {
+  return (min(size, (1 << 19) - 1) << 12) | (4095 - q);
+}
+
+template <typename I>
+__device__ bool schedule_items_small(const SchedParams& p, UnitInfo i, I W, long long* red, int4* pcs,
+                                     int* scratch) {
+  const int tid = threadIdx.x;
+  const int u = tid;
+  int* unit_k = scratch;                      // [kThreads] pieces of unit u
+  int* unit_slot = scratch + kThreads;        // [kThreads] its first partial slot (-1)
+  // [kSmallPieces + 4] order keys: larger = earlier in the list (size in
+  // groups, then list order), -1 past the last piece
+  int* pkey = scratch + 2 * kThreads;
+  int* ptile = pkey + kSmallPieces + 4;       // [kSmallPieces + 4] row tiles (items) of each piece
+  I sum;
+  const I pos = block_exclusive_scan<I>(static_cast<I>(i.groups), red, &sum);
+  Cuts<I> c{0, 0};
+  if (i.tiles > 0 && i.groups > 1) c = row_cuts<I>(pos, static_cast<I>(i.groups), W);
+  const int k = i.tiles > 0 ? c.count + 1 : 0;
+  int3 tot;
+  const int3 base = block_exclusive_scan3(make_int3(k, k > 1 ? k * i.tiles : 0, k * i.tiles),
+                                          reinterpret_cast<int3*>(red + kThreads / 32), &tot);
+  if (tot.x > kSmallPieces) return false;  // the same for every thread
+  if (k > 0) {
+    unit_k[u] = k;
+    unit_slot[u] = k > 1 ? base.y : -1;
+    int prev = 0;
+#pragma unroll 1
+    for (int j = 0; j < k; ++j) {
+      const int next = j < c.count ? static_cast<int>(c.first + static_cast<I>(j) * W - pos) : i.groups;
+      pcs[base.x + j] = make_int4(next - prev, u, prev, j);
+      pkey[base.x + j] = order_key(next - prev, base.x + j);
+      ptile[base.x + j] = i.tiles;
+      prev = next;
+    }
+#pragma unroll 1
+    for (int t = 0; t < i.tiles; ++t)
+      reinterpret_cast<int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + t] =
+          make_int2(k > 1 ? base.y + t * k : -1, k);
+  }
+  const int P = tot.x;
+  if (tid < 4) {  // pad to whole int4s: before no piece
+    pkey[P + tid] = -1;
+    ptile[P + tid] = 0;
+  }
+  __syncthreads();
+  const int4* pk4 = reinterpret_cast<const int4*>(pkey);
+  const int4* pt4 = reinterpret_cast<const int4*>(ptile);
+#pragma unroll 1
+  for (int q = tid; q < P; q += kThreads) {
+    const int4 me = pcs[q];
+    const int kq = pkey[q];
+    // items of the pieces before this one (one compare per piece, no branch)
+    int at = 0;
+#pragma unroll 4
+    for (int o = 0; o < P; o += 4) {
+      const int4 a = pk4[o >> 2];
+      const int4 b = pt4[o >> 2];
+      at += a.x > kq ? b.x : 0;
+      at += a.y > kq ? b.y : 0;
+      at += a.z > kq ? b.z : 0;
+      at += a.w > kq ? b.w : 0;
+    }
+    const int T = ptile[q], km = unit_k[me.y], slot0 = unit_slot[me.y];
+    const int kb = static_cast<int>(min(static_cast<long long>(me.z) * kGroupKeys, static_cast<long long>(INT32_MAX)));
+    const int ke =
+        static_cast<int>(min(static_cast<long long>(me.z + me.x) * kGroupKeys, static_cast<long long>(INT32_MAX)));
+#pragma unroll 1
+    for (int t = 0; t < T; ++t) {
+      int4* it = reinterpret_cast<int4*>(p.items) + 2 * static_cast<int64_t>(at + t);
+      it[0] = make_int4(me.y, t, kb, ke);
+      it[1] = make_int4(km > 1 ? slot0 + t * km + me.w : -1, 0, 0, 0);
+    }
+  }
+  if (tid == 0) *p.n_items = tot.z;
+  return true;
+}
+
 // Contiguous mode: items in sequence order and each worker's first item.
 template <typename I, typename Info>
 __device__ void schedule_contiguous(const SchedParams& p, Info info, I W, int workers, long long* red,
@@ -301,9 +429,9 @@ __device__ void schedule_contiguous(const SchedParams& p, Info info, I W, int wo
 __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams p) {
   // the decode kernel may launch now; it waits for this grid before reading
   asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-  __shared__ long long red[kThreads / 32];
-  __shared__ int hist[kSizeBins];
-  __shared__ int start[kSizeBins];
+  __shared__ long long red[kThreads / 32 * 3];  // block_exclusive_scan3 uses the last 16 as int3[8]
+  __shared__ __align__(16) int hist[kSizeBins];
+  __shared__ __align__(16) int start[kSizeBins];
   __shared__ int cache_g[kCacheUnits];
   __shared__ int cache_t[kCacheUnits];
   const int tid = threadIdx.x;
@@ -336,6 +464,13 @@ __global__ void __launch_bounds__(kThreads, 1) schedule_kernel(const SchedParams
   }
   const long long workers = p.workers > 0 ? p.workers : 1;
   const long long W = total > 0 ? (total + workers - 1) / workers : 1;
+  if (U <= kThreads && total < (1ll << 30)) {
+    static_assert(kSmallPieces * 16 <= kSizeBins * 4 && 2 * kThreads + 2 * (kSmallPieces + 4) <= kSizeBins,
+                  "small-list scratch");
+    const UnitInfo mine = tid < U ? UnitInfo{cache_g[tid], cache_t[tid]} : UnitInfo{0, 0};
+    if (schedule_items_small<int>(p, mine, static_cast<int>(W), red, reinterpret_cast<int4*>(hist), start))
+      return;
+  }
   if (total < (1ll << 30))
     schedule_items<int>(p, info, static_cast<int>(W), red, hist, start);
   else
