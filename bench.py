@@ -128,18 +128,18 @@ def _flops(w):
 PROFILED_TRAFFIC = {
     (4, "dsv3", None): {  # decode_tc.cu, DeepSeek-V3-shaped batch (profiles/decode_tc_dsv3.md)
         "source": "decode_tc.cu",
-        "code_sha256": "6ed484883791543c30f67ace22adb9950df6008e8220e28377dfbfbb134d6d79",
-        "dram_per_alg_byte": (139.582976 + 3.517184) / 138.103440,
+        "code_sha256": "8627e3e3dff2a7f099e4577878849af60304b92bd461a6cd133bfca0f5975a21",
+        "dram_per_alg_byte": (139.609088 + 3.360256) / 138.103440,
     },
     (5, "fp8", 16): {  # decode_hn.cu, e4m3 batch at 16 heads (profiles/decode_hn_fp8.md)
         "source": "decode_hn.cu",
-        "code_sha256": "6dc1a0e376477084d95e203f130c7803da11a6b501982c01d9a77f70799d2fe9",
-        "dram_per_alg_byte": (226.829824 + 3.939840) / 226.738272,
+        "code_sha256": "b27dd235d6d48fcd1daf6457f627d20b78edd5858b4d37eb289261f2ff1ad65b",
+        "dram_per_alg_byte": (226.828800 + 3.769344) / 226.738272,
     },
     (5, "fp8", 128): {  # decode_hn.cu on CTA-pair clusters, e4m3 batch at 128 heads (same file)
         "source": "decode_hn.cu",
-        "code_sha256": "6dc1a0e376477084d95e203f130c7803da11a6b501982c01d9a77f70799d2fe9",
-        "dram_per_alg_byte": (228.408832 + 4.478464) / 228.286560,
+        "code_sha256": "b27dd235d6d48fcd1daf6457f627d20b78edd5858b4d37eb289261f2ff1ad65b",
+        "dram_per_alg_byte": (228.402432 + 4.709632) / 228.286560,
     },
 }
 
