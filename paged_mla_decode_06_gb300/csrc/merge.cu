@@ -43,9 +43,6 @@ __device__ __forceinline__ int part_len_of(const PartLens& pl, int t) {
 
 template <int VPL>  // float4 values per lane: rank / 128
 __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeParams p) {
-  // launched as a programmatic dependent of the decode under the balanced
-  // schedule: wait for it to complete (a no-op after an ordinary launch)
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int lane = threadIdx.x & 31;
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
   const int64_t total = static_cast<int64_t>(p.num_tokens) * p.num_heads;
@@ -57,7 +54,11 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
   if (p.unit_tab != nullptr) {
     // balanced schedule: the rows of a (unit, row tile) split into k > 1
     // pieces own k consecutive slots of tile_rows rows; k == 1 rows were
-    // written by the decode kernel itself
+    // written by the decode kernel itself. The unit table comes from the
+    // schedule kernel, which completed before the decode began, so it is
+    // read while the decode (this grid's programmatic primary) may still
+    // run, and a row that was not split leaves at once; only the partials
+    // wait for the decode to complete.
     int u = t, tok0 = t;
     if (!p.sparse && p.part.qo_indptr != nullptr) {
       u = request_of(p.part, t);
@@ -65,13 +66,17 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) merge_kernel(const MergeP
     }
     const int r = (t - tok0) * p.num_heads + h;
     const int tr = p.tile_rows;
-    if (r / tr >= p.tiles_max) return;
-    const int2 e = reinterpret_cast<const int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + r / tr];
+    int2 e = make_int2(-1, 0);
+    if (r / tr < p.tiles_max)
+      e = reinterpret_cast<const int2*>(p.unit_tab)[static_cast<int64_t>(u) * p.tiles_max + r / tr];
     if (e.y <= 1) return;
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     merge_row<VPL, true>(p.segm_out, p.segm_max, p.segm_expsum, static_cast<int64_t>(e.x) * tr + r % tr,
                          tr, e.y, sink2, out, p.lse + gw, lane);
     return;
   }
+  // uniform partition: an ordinary launch (the wait is a no-op)
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
   const int NS = p.num_segments;
   const int len = part_len_of(p.part, t);
   const int span = NS * p.tile_size;
