@@ -21,8 +21,16 @@ TOL_LSE = 1e-3
 # probability rounded to bf16 moves the output by up to another 2^-8 * 4.5
 # when only a couple of keys carry the weight; such rows are held to
 # TOL_FEW_KEYS = 3e-2.
+# The key count is a proxy for that concentration: a row's scores vary with
+# its q, and a row of a few hundred keys can still put its weight on two or
+# three of them. The direct sign is the row's exact output: the mean of >= 12
+# unit-variance values passes DIFFUSE_MAX = 1.5 in a given column about once
+# in five million draws, so a (token, head) row whose oracle output exceeds
+# it anywhere is held like a row of few keys (seen: rows of 261-431 keys with
+# |out| of 2.2-3.3, where bf16's half unit in the last place alone is 0.0078).
 FEW_KEYS = 256
 TOL_FEW_KEYS = 3e-2
+DIFFUSE_MAX = 1.5
 
 
 def run_gpu(w, num_segments=None, stream=None, kernel=B.MLA_KERNEL_AUTO):
@@ -75,10 +83,12 @@ def visible_keys(w, tokens=None, slots=None, indptr=None):
 
 
 def assert_close(out, lse, ref_out, ref_lse, dtype="bf16", what="", keys=None):
-    """Element-wise comparison, tolerance per row: rows of tokens that see at
-    least FEW_KEYS keys (or every row when ``keys`` is None) are held to the
-    workload bound TOL_OUT[dtype]; rows of fewer keys to TOL_FEW_KEYS. LSE to
-    TOL_LSE everywhere. Returns the largest error over the strict rows."""
+    """Element-wise comparison, tolerance per (token, head) row: rows of
+    tokens that see at least FEW_KEYS keys (or every row when ``keys`` is
+    None) and whose exact output stays within DIFFUSE_MAX are held to the
+    workload bound TOL_OUT[dtype]; rows of fewer keys, or dominated by a few
+    values, to TOL_FEW_KEYS. LSE to TOL_LSE everywhere. Returns the largest
+    error over the strict rows."""
     assert out.shape == ref_out.shape, (out.shape, ref_out.shape)
     assert np.isfinite(out).all(), f"{what}: non-finite output"
     T = out.shape[0]
@@ -86,14 +96,18 @@ def assert_close(out, lse, ref_out, ref_lse, dtype="bf16", what="", keys=None):
         keys = np.full(T, np.iinfo(np.int64).max)
     keys = np.asarray(keys)
     assert keys.shape == (T,), (keys.shape, T)
-    row_err = np.abs(out - ref_out).reshape(T, -1).max(axis=1) if out.size else np.zeros(T)
-    strict = keys >= FEW_KEYS
+    width = out.shape[-1] if out.ndim >= 2 else 1
+    o = out.reshape(T, -1, width)
+    r = ref_out.reshape(T, -1, width)
+    row_err = np.abs(o - r).max(axis=2) if out.size else np.zeros((T, 1))
+    mag = np.abs(r).max(axis=2) if out.size else np.zeros((T, 1))
+    strict = (keys[:, None] >= FEW_KEYS) & (mag <= DIFFUSE_MAX)
     tol = np.where(strict, TOL_OUT[dtype], TOL_FEW_KEYS)
-    bad = np.nonzero(row_err > tol)[0]
+    bad = np.argwhere(row_err > tol)
     if bad.size:
-        worst = sorted(bad, key=lambda t: -row_err[t])[:5]
-        msg = ", ".join(f"token {t}: {row_err[t]:.3e} > {tol[t]:.0e} ({keys[t]} keys)"
-                        for t in worst)
+        worst = sorted(map(tuple, bad), key=lambda th: -row_err[th])[:5]
+        msg = ", ".join(f"token {t} head {h}: {row_err[t, h]:.3e} > {tol[t, h]:.0e} "
+                        f"({keys[t]} keys, max |oracle| {mag[t, h]:.2f})" for t, h in worst)
         raise AssertionError(f"{what}: max |out - oracle| per row: {msg}")
     ninf = np.isneginf(ref_lse)
     assert np.array_equal(np.isneginf(lse), ninf), f"{what}: -inf lse pattern differs"

@@ -190,7 +190,7 @@ def test_tcgen05_head_counts_and_short_rows(heads):
     assert_close(out, lse, ref_o, ref_l, "bf16", f"tcgen05 H={heads}", keys=visible_keys(w))
 
 
-@pytest.mark.parametrize("case", ["dense", "multi_token", "sparse", "one_long"])
+@pytest.mark.parametrize("case", ["dense", "multi_token", "sparse", "one_long", "many_units"])
 def test_balanced_schedule_items(case):
     """The planner's balanced schedule (tensor-core kernel, segments left to
     the planner): read the work list back from the workspace and check that
@@ -212,6 +212,12 @@ def test_balanced_schedule_items(case):
     elif case == "one_long":       # one request cut into pieces on every pair
         w = I.build_dense(73, seq_lens=[60000], num_heads=128, block_size=64, num_segments=0)
         lens, tiles = w.seq_lens, np.ones(1, dtype=np.int64)
+    elif case == "many_units":     # more units than the schedule block's threads: the binned path
+        rng = np.random.default_rng(74)
+        lens = rng.integers(0, 700, size=300)
+        lens[:3] = [0, 1, 4000]
+        w = I.build_dense(74, seq_lens=lens.tolist(), num_heads=128, block_size=64, num_segments=0)
+        lens, tiles = w.seq_lens, np.ones(len(lens), dtype=np.int64)
     else:
         w = I.sparse_topk(num_reqs=2, tokens_per_req=3, cache_tokens=4096, topk=1024,
                           max_pad=300, num_segments=0)
@@ -266,6 +272,17 @@ def test_balanced_schedule_items(case):
     assert split or case == "sparse" or n == sum(int(t) for t in tiles)
     ref_o, ref_l = run_oracle(w)
     assert_close(out, lse, ref_o, ref_l, "bf16", f"balanced {case}", keys=visible_keys(w))
+    # the list again from the same lengths: the same items, and in the same
+    # order when the units fit the schedule block's threads (pieces ranked by
+    # a key; the binned path for more units orders equal sizes by atomics)
+    B.mla_decode_schedule(plan, seq_lens=None if w.sparse else dw.seq_lens, qo_indptr=dw.qo_indptr,
+                          workspace=dw.workspace)
+    torch.cuda.synchronize()
+    items2 = dw.workspace.cpu().numpy()[512:512 + 32 * n].view(np.int32).reshape(n, 8)
+    if len(lens) <= 256:
+        assert np.array_equal(items2, items)
+    else:
+        assert sorted(map(tuple, items2.tolist())) == sorted(map(tuple, items.tolist()))
     # the same work list serves a second decode: identical bits
     dw.out.zero_()
     dw.lse.zero_()
