@@ -171,7 +171,9 @@ typedef struct {
  * g = cdiv(len, 128) key groups are laid end to end and the sequence of all
  * groups is cut every W = cdiv(total, workers) groups. CTA-pair kernel:
  * workers = num_sms / 2 pairs, cuts within W / 8 of a row's ends dropped,
- * one item per pair, the pieces longest first. Rows-as-N kernel: workers =
+ * one item per pair, the pieces longest first (pieces of equal size in
+ * unit order when the units number at most 256, so the list is the same on
+ * every call; larger batches order them arbitrarily). Rows-as-N kernel: workers =
  * num_sms CTAs (or the clusters of two that fit), every cut kept, and
  * worker w runs the pieces of groups [w W, (w + 1) W) one after another.
  * max_items = rows + workers. Unsplit rows are written by the decode kernel
