@@ -15,7 +15,7 @@ from paged_mla_decode_06_gb300 import binding as B
 from paged_mla_decode_06_gb300 import build as BUILD
 from paged_mla_decode_06_gb300 import inputs as I
 from tests.gpu_helpers import assert_close, oracle_slots, run_gpu, run_oracle, visible_keys
-from tests.test_schedule_rule import cut_rule
+from tests.test_schedule_rule import cut_rule, ranked_list
 
 pytestmark = pytest.mark.gpu
 
@@ -262,6 +262,12 @@ def test_balanced_schedule_items(case):
             mine = mine[np.argsort(mine[:, 2])]
             assert ((mine[:, 3] - mine[:, 2]) // 128).tolist() == pieces_m[r], (u, t)
             r += 1
+    # at most 256 units: the device's list is the host model's, item by item
+    # (pieces by size, ties in unit order; the sparse units are its tokens)
+    if len(lens) <= 256:
+        want = ranked_list(groups, [int(t) for t in tiles], plan.split_items // (2 * per_cut))
+        got = [(int(a), int(b), int(c), int(d), int(e)) for a, b, c, d, e in items[:, :5]]
+        assert got == want
     # a piece's row tiles are consecutive items
     for i in range(n):
         u, t, kb = items[i, 0], items[i, 1], items[i, 2]

@@ -40,6 +40,55 @@ def cut_rule(groups, tiles, pairs):
     return rows, pieces, W
 
 
+def ranked_list(groups, tiles, pairs):
+    """The list a batch of at most 256 units gets: the cut rule's pieces,
+    enumerated unit by unit (piece j of unit u), ordered by size, largest
+    first, ties in enumeration order; a piece's T row tiles are consecutive
+    items. A split unit (k > 1 pieces) owns k T partial slots from the prefix
+    over the units before it, tile t's piece j at slot base + t k + j.
+    Returns (unit, tile, first key, end key, slot or -1) per item."""
+    _, pieces, _ = cut_rule(groups, tiles, pairs)
+    enum, base, r = [], 0, 0
+    for u, (g, t) in enumerate(zip(groups, tiles)):
+        if t == 0:
+            continue
+        sizes = pieces[r]
+        r += t
+        k = len(sizes)
+        edge = 0
+        for j, size in enumerate(sizes):
+            enum.append((size, u, t, edge, j, k, base))
+            edge += size
+        if k > 1:
+            base += k * t
+    order = sorted(range(len(enum)), key=lambda i: (-enum[i][0], i))
+    items = []
+    for i in order:
+        size, u, t, edge, j, k, b = enum[i]
+        for tt in range(t):
+            items.append((u, tt, edge * 128, (edge + size) * 128, b + tt * k + j if k > 1 else -1))
+    return items
+
+
+@pytest.mark.parametrize("name", ["equal", "one_long", "zeros", "mixed_tiles"])
+def test_ranked_list_covers_every_row_once(name):
+    """The small-batch list is a permutation of the cut rule's pieces, its
+    sizes never grow, and the split units' slots are distinct."""
+    groups, tiles = CASES[name]
+    items = ranked_list(groups, tiles, 76)
+    _, pieces, _ = cut_rule(groups, tiles, 76)
+    assert len(items) == sum(len(p) for p in pieces)
+    sizes = [(ke - kb) // 128 for _, _, kb, ke, _ in items]
+    assert all(a >= b for a, b in zip(sizes, sizes[1:]))
+    slots = [s for *_, s in items if s >= 0]
+    assert len(set(slots)) == len(slots)
+    for u, (g, t) in enumerate(zip(groups, tiles)):
+        for tt in range(t):
+            mine = sorted((kb, ke) for uu, ti, kb, ke, _ in items if uu == u and ti == tt)
+            assert mine[0][0] == 0 and mine[-1][1] == g * 128
+            assert all(a[1] == b[0] for a, b in zip(mine, mine[1:]))
+
+
 CASES = {
     "equal": ([128] * 52, [1] * 52),
     "one_long": ([8192], [1]),
